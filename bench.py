@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""MoE-layer forward throughput on GB300 (tokens/s) with its roofline fraction.
+
+One step = one moe_forward_ex call over one batch of a synthetic workload: gate
++ top-k + FP8 quantisation, dispatch plan, dispatch copy, grouped GEMM1 (SwiGLU,
+FP8 re-quantisation), grouped GEMM2 and the combine -- every stage of the layer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+  python bench.py --impl reference ...     # the CPU oracle on the host cores
+
+Timing: W untimed warm-up steps, then K steps, each timed with CUDA events on
+the launching stream (the library records one event between every two stages),
+with a 256 MiB write between steps to flush L2; barrier + synchronize on both
+sides of the timed loop; the per-step time is the max over ranks.  Under
+torchrun (N > 1) every rank runs its own replica of the workload (token-sharded
+data parallelism: there is no exchange between ranks), so scaling is weak.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec at 1 GB300; achieved TFLOP/s or HBM GB/s as % of roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0           # nominal dense FP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_setup(want_nccl=True):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (want_nccl and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def dist_max(v, device):
+    """Max of a float over ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", FALLBACK_HBM_GBS), d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), \
+            d.get("bf16_tflops_sustained"), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profile_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    if there is none or the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    src = os.path.join(ROOT, "fp4_expert_grouped_gb300", "csrc", "gemm.cu" if "gemm" in kernel else "kernels.cu")
+    if vals.get("source_sha") != file_sha(src):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------------- accounting
+
+def weight_bytes_per_expert(d, inter):
+    """FP4 codes (1/2 byte) + UE8M0 scales (1/32 byte) of W13 and W2."""
+    return 3 * d * inter // 2 + 3 * d * inter // 32
+
+
+def gemm_bytes(w, touched, which):
+    """Algorithmic bytes of one grouped-GEMM launch: the touched experts' packed
+    weights read once, the pair rows read once, the outputs written once."""
+    d, I, P = w.d, w.inter, w.P
+    if which == "gemm1":
+        wb = touched * (2 * I * d // 2 + 2 * I * d // 32)
+        return wb + P * d + P * (d // 128) + P * I + P * (I // 128)
+    wb = touched * (d * I // 2 + d * I // 32)
+    return wb + P * I + P * (I // 128) + P * d * 2
+
+
+def gemm_flops(w, which):
+    return 2 * w.P * w.d * (2 * w.inter if which == "gemm1" else w.inter)
+
+
+def layer_roofline(w, touched, hbm_gbs, fp8_tflops):
+    """The layer's roofline time (us): the slower of 6*d*I FLOPs per pair at the
+    FP8 peak and (touched weights + x + out + gate_w) bytes at HBM bandwidth."""
+    flops = 6.0 * w.d * w.inter * w.P
+    byts = touched * weight_bytes_per_expert(w.d, w.inter) + 2 * w.T * w.d * 2 + w.d * w.E * 4
+    t_f = flops / (fp8_tflops * 1e12) * 1e6
+    t_b = byts / (hbm_gbs * 1e9) * 1e6
+    return max(t_f, t_b), ("tensor" if t_f > t_b else "hbm"), flops, byts
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, x, gw, bias, n_tok, seed=12345):
+    """Time the CPU oracle on a seeded sample of n_tok tokens of the workload.
+    Returns (seconds, tokens, cores).  The oracle packs the experts those tokens
+    route to from the same fp32 weights (regenerated on the device)."""
+    import oracle
+    from fp4_expert_grouped_gb300 import inputs
+    rng = np.random.default_rng(seed)
+    tokens = np.sort(rng.choice(w.T, min(n_tok, w.T), replace=False)).astype(np.int32)
+    xb = inputs.bf16_bits(x)
+    gwn = gw.detach().cpu().numpy()
+    bn = None if bias is None else bias.detach().cpu().numpy()
+    ridx, _ = oracle.route(xb[tokens], gwn, w.k, bn)
+    f13 = np.zeros((w.E, 2 * w.inter, w.d // 2), np.uint8)
+    s13 = np.zeros((w.E, 2 * w.inter, w.d // 32), np.uint8)
+    f2 = np.zeros((w.E, w.d, w.inter // 2), np.uint8)
+    s2 = np.zeros((w.E, w.d, w.inter // 32), np.uint8)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    for e in sorted(set(ridx.reshape(-1).tolist())):
+        a, b = inputs.make_expert(w, e, gen_dev)
+        r13 = oracle.pack_fp4(a.cpu().numpy()[None])
+        r2 = oracle.pack_fp4(b.cpu().numpy()[None])
+        f13[e], s13[e] = r13[0][0], r13[1][0]
+        f2[e], s2[e] = r2[0][0], r2[1][0]
+    t0 = time.perf_counter()
+    oracle.moe_forward(xb, gwn, f13, s13, f2, s2, w.k, bn, tokens=tokens)
+    dt = time.perf_counter() - t0
+    return dt, len(tokens), oracle.num_threads()
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, w, ws_, rank):
+    if rank != 0:
+        return
+    from fp4_expert_grouped_gb300 import inputs
+    import oracle
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x, gw, b = inputs.make_x_gate(w, dev)
+    cores = oracle.num_threads()
+    n_tok = max(1, min(w.T, cores))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, gw, b, 1, seed=999)
+    times = []
+    for s in range(args.steps):
+        dt, n, _ = oracle_sample(w, x, gw, b, n_tok, seed=1000 + s)
+        times.append(dt / n)
+    per_tok = statistics.mean(times)
+    value = 1.0 / per_tok
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * n_tok * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 accumulate (oracle)", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d seeded tokens per step of the %s workload" % (n_tok, w.name)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "T": w.T, "d": w.d, "inter": w.inter, "E": w.E, "k": w.k,
+            "zipf_bias": w.zipf_bias, "seed": w.seed,
+            "l2": "flushed (256 MiB write) before every timed step; weights %.2f GB >> 129 MB L2"
+                  % (w.E * weight_bytes_per_expert(w.d, w.inter) / 1e9)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, w, world, rank, local):
+    from fp4_expert_grouped_gb300 import capi, inputs, layer
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_gbs, bf16_tflops, bf16_sust, peak_src = measured_peaks()
+    fp8_tflops = bf16_tflops * FP8_OVER_BF16
+
+    x, gw, bias = inputs.make_x_gate(w, dev)
+    pk = layer.pack_workload(w, dev)
+    ws = layer.workspace(w.T, w.d, w.inter, w.E, w.k, dev)
+    out = torch.empty_like(x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nst = len(capi.STAGES)
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+        for e in evs:
+            e.record(stream)          # materialise the event handles
+        return evs
+
+    def step(evs):
+        capi.moe_forward_ex(x, gw, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, out, w.k,
+                            stream=stream, gate_bias=bias, workspace=ws, stage_events=evs)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(None)
+    torch.cuda.synchronize(dev)
+    st = capi.moe_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status after warm-up: " + capi.moe_status_string(st))
+
+    events = [new_events() for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    dist_barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    for s in range(args.steps):
+        flush.zero_()
+        step(events[s])
+    torch.cuda.synchronize(dev)
+    dist_barrier()
+    ck = clocks.stop()
+    st = capi.moe_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status after timed steps: " + capi.moe_status_string(st))
+
+    step_ms = [events[s][0].elapsed_time(events[s][nst]) for s in range(args.steps)]
+    stage_ms = {name: statistics.mean(events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps))
+                for i, name in enumerate(capi.STAGES)}
+    ms_local = statistics.mean(step_ms)
+    ms = dist_max(ms_local, dev)
+    value = world * w.T / (ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_ms = []
+    for s in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.copy_(x_host, non_blocking=True)
+        step(None)
+        out_host.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_v = world * w.T / (dist_max(statistics.mean(e2e_ms), dev) / 1e3)
+
+    # ---- roofline of the dominant kernel and of the layer
+    total, off, strides = capi.moe_workspace_layout(w.T, w.d, w.inter, w.E, w.k)
+    offs = ws[off[capi.MOE_WS_EXPERT_OFFSETS]:off[capi.MOE_WS_EXPERT_OFFSETS] + 4 * (w.E + 1)].cpu().numpy()
+    counts = np.diff(offs.view(np.int32))
+    touched = int(np.count_nonzero(counts))
+    dom = max(("gemm1", "gemm2"), key=lambda k: stage_ms[k])
+    dom_ms = stage_ms[dom]
+    fl = gemm_flops(w, dom)
+    by = gemm_bytes(w, touched, dom)
+    t_f = fl / (fp8_tflops * 1e12)
+    t_b = by / (hbm_gbs * 1e9)
+    if t_f > t_b:
+        peak = fp8_tflops
+        roof = {"bound": "tensor", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": peak, "unit": "TFLOP/s"}
+        roof["peak_note"] = "FP8 = %.1f x %s bf16 burst" % (FP8_OVER_BF16, peak_src)
+    else:
+        peak = hbm_gbs
+        roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s"}
+        roof["peak_note"] = "%s copy bandwidth" % peak_src
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["algorithmic_bytes_per_launch"] = by
+    roof["algorithmic_flops_per_launch"] = fl
+    roof["traffic"] = profile_traffic(dom, w.name)
+    t_roof_us, lbound, lflops, lbytes = layer_roofline(w, touched, hbm_gbs, fp8_tflops)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 x fp4_e2m1 (fp32 accumulate)",
+        "data": "synthetic: seeded normal x / gate_w, N(0,1/fan_in) fp32 expert weights packed to MXFP4 on the GPU",
+        "config": config_of(w),
+        "roofline": roof,
+        "layer": {"roofline_us": t_roof_us, "bound": lbound, "frac": t_roof_us / (ms * 1e3),
+                  "weight_GBps": touched * weight_bytes_per_expert(w.d, w.inter) / (ms / 1e3) / 1e9,
+                  "TFLOPs": lflops / (ms / 1e3) / 1e12, "touched_experts": touched,
+                  "max_expert_load": int(counts.max()), "mean_expert_load": float(counts.mean())},
+        "stages_us": {k: v * 1e3 for k, v in stage_ms.items()},
+        "e2e": {"value": e2e_v, "unit": UNIT, "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+        "gpu_launches": len(capi.STAGES) * args.steps,
+        "clocks": ck,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, n, cores = oracle_sample(w, x, gw, bias, n_tok=max(1, min(w.T, 2 * os.cpu_count())))
+        line["cpu_baseline"] = {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": "%d seeded tokens of the %s workload (oracle time %.1f s)"
+                                          % (n, w.name, dt)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from fp4_expert_grouped_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    world, rank, local = dist_setup(want_nccl=(args.impl == "ours"))
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+    else:
+        run_ours(args, w, world, rank, local)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

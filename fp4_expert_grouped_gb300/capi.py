@@ -1,0 +1,177 @@
+"""Thin ctypes binding of libfp4moe.so (include/fp4moe.h), same names.
+
+Argument marshalling only: torch tensors become device pointers and the current
+torch stream becomes the cudaStream_t; every step of the layer runs in the
+library's CUDA kernels.  If the library has not been built, importing this
+module raises -- there is no other implementation to fall back to.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfp4moe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libfp4moe.so is not built (%s); run fp4_expert_grouped_gb300/build.py "
+                      "or __graft_entry__.build()" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_CUDA",
+    4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_UNSUPPORTED_DEVICE", 7: "MOE_ERR_DEVICE_FAULT",
+}
+STAGES = ["gate", "topk", "plan", "dispatch", "gemm1", "gemm2", "combine"]
+(MOE_WS_XQ, MOE_WS_XS, MOE_WS_LOGITS, MOE_WS_TOPK_IDX, MOE_WS_TOPK_W, MOE_WS_EXPERT_OFFSETS,
+ MOE_WS_SORTED_PAIR, MOE_WS_PAIR_POS, MOE_WS_TILE_PREFIX, MOE_WS_HQ, MOE_WS_HS, MOE_WS_Y,
+ MOE_WS_XQ_SORTED, MOE_WS_XS_SORTED, MOE_WS_COUNT) = range(15)
+
+# every symbol the header declares
+EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_quantize_act", "moe_route",
+           "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
+           "moe_workspace_layout", "moe_get_device_status"]
+
+
+class MoeForwardOpts(ctypes.Structure):
+    _fields_ = [("gate_bias", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("topk_idx_out", ctypes.c_void_p),
+                ("topk_w_out", ctypes.c_void_p), ("pair_pos_out", ctypes.c_void_p),
+                ("flags", ctypes.c_uint32), ("stage_events", ctypes.POINTER(ctypes.c_void_p))]
+
+
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_lib.moe_status_string.argtypes = [_i]
+_lib.moe_status_string.restype = ctypes.c_char_p
+_lib.moe_version.argtypes = []
+_lib.moe_version.restype = _i
+_lib.moe_pack_fp4.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp]
+_lib.moe_pack_fp4.restype = _i
+_lib.moe_quantize_act.argtypes = [_vp, _vp, _vp, _i, _i, _vp]
+_lib.moe_quantize_act.restype = _i
+_lib.moe_route.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+_lib.moe_route.restype = _i
+_lib.moe_dispatch_plan.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]
+_lib.moe_dispatch_plan.restype = _i
+_lib.moe_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+_lib.moe_forward.restype = _i
+_lib.moe_forward_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
+                                ctypes.POINTER(MoeForwardOpts)]
+_lib.moe_forward_ex.restype = _i
+_lib.moe_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+_lib.moe_workspace_size.restype = _sz
+_lib.moe_workspace_layout.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]
+_lib.moe_workspace_layout.restype = _sz
+_lib.moe_get_device_status.argtypes = [_vp]
+_lib.moe_get_device_status.restype = _i
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__("%s failed: %s" % (what, STATUS_NAMES.get(code, code)))
+
+
+def lib():
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code, what):
+    if code != MOE_OK:
+        raise MoeError(code, what)
+
+
+def moe_status_string(code):
+    return _lib.moe_status_string(code).decode()
+
+
+def moe_version():
+    return _lib.moe_version()
+
+
+def moe_pack_fp4(w, w_fp4, w_scale, stream=None):
+    """w fp32 [E, N, K] -> w_fp4 uint8 [E, N, K/2], w_scale uint8 [E, N, K/32] (device tensors)."""
+    E, N, K = w.shape if w.dim() == 3 else (1, *w.shape)
+    _check(_lib.moe_pack_fp4(_ptr(w), _ptr(w_fp4), _ptr(w_scale), E, N, K, _stream(stream)), "moe_pack_fp4")
+
+
+def moe_quantize_act(x, xq, xs, stream=None):
+    T, d = x.shape
+    _check(_lib.moe_quantize_act(_ptr(x), _ptr(xq), _ptr(xs), T, d, _stream(stream)), "moe_quantize_act")
+
+
+def moe_route(x, gate_w, gate_bias, topk_idx, topk_w, stream=None):
+    T, d = x.shape
+    E = gate_w.shape[1]
+    k = topk_idx.shape[1]
+    _check(_lib.moe_route(_ptr(x), _ptr(gate_w), _ptr(gate_bias), _ptr(topk_idx), _ptr(topk_w),
+                          T, d, E, k, _stream(stream)), "moe_route")
+
+
+def moe_dispatch_plan(topk_idx, expert_offsets, sorted_pair, pair_pos, E, stream=None):
+    T, k = topk_idx.shape
+    _check(_lib.moe_dispatch_plan(_ptr(topk_idx), _ptr(expert_offsets), _ptr(sorted_pair), _ptr(pair_pos),
+                                  T, E, k, _stream(stream)), "moe_dispatch_plan")
+
+
+def moe_workspace_size(T, d, inter, E, k):
+    return _lib.moe_workspace_size(T, d, inter, E, k)
+
+
+def moe_workspace_layout(T, d, inter, E, k):
+    """Return (total_bytes, offsets[list], strides[list])."""
+    off = (_sz * MOE_WS_COUNT)()
+    st = (_sz * MOE_WS_COUNT)()
+    total = _lib.moe_workspace_layout(T, d, inter, E, k, off, st)
+    return total, list(off), list(st)
+
+
+def moe_forward(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stream=None):
+    T, d = x.shape
+    E = gate_w.shape[1]
+    inter = w13_fp4.shape[1] // 2
+    _check(_lib.moe_forward(_ptr(x), _ptr(gate_w), _ptr(w13_fp4), _ptr(w13_scale), _ptr(w2_fp4),
+                            _ptr(w2_scale), _ptr(out), T, d, inter, E, k, _stream(stream)), "moe_forward")
+
+
+def moe_forward_ex(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stream=None, gate_bias=None,
+                   workspace=None, topk_idx_out=None, topk_w_out=None, pair_pos_out=None, flags=0,
+                   stage_events=None):
+    """stage_events: optional list of len(STAGES) + 1 recorded torch.cuda.Event objects."""
+    T, d = x.shape
+    E = gate_w.shape[1]
+    inter = w13_fp4.shape[1] // 2
+    evs = None
+    if stage_events is not None:
+        assert len(stage_events) == len(STAGES) + 1
+        evs = (ctypes.c_void_p * len(stage_events))(*[ev.cuda_event for ev in stage_events])
+    o = MoeForwardOpts(_ptr(gate_bias), _ptr(workspace),
+                       0 if workspace is None else workspace.numel() * workspace.element_size(),
+                       _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(pair_pos_out), flags,
+                       ctypes.cast(evs, ctypes.POINTER(ctypes.c_void_p)) if evs is not None else None)
+    _check(_lib.moe_forward_ex(_ptr(x), _ptr(gate_w), _ptr(w13_fp4), _ptr(w13_scale), _ptr(w2_fp4),
+                               _ptr(w2_scale), _ptr(out), T, d, inter, E, k, _stream(stream),
+                               ctypes.byref(o)), "moe_forward_ex")
+
+
+def moe_get_device_status(stream=None):
+    """Synchronise the stream and return (and clear) the device status code."""
+    return _lib.moe_get_device_status(_stream(stream))

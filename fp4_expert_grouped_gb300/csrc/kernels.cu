@@ -1,0 +1,570 @@
+// kernels.cu -- the CUDA-core stages of the MoE layer forward:
+//   MXFP4 weight packing, FP8 E4M3 activation quantisation, fixed-order gate
+//   logits, warp-level top-k with sqrt(softplus) weights, the stable
+//   counting-sort dispatch plan, the dispatch copy into expert order and the
+//   slot-order combine.
+//
+// Sources: "DeepSeek-V4揭秘：细粒度专家并行隐藏通信时延，FP4量化与TileLang协同优化百万Token上下文"
+// (itsolotime.com/archives/32374): section 1.1 (dispatch / combine stages),
+// 1.4 (FP8 dispatch, BF16 combine), 3.1-3.2 (batch invariance, no
+// atomic-order-dependent sums), 4 (MXFP4 expert weights).
+// "DeepSeek V4架构学习笔记" (67808.cn/a/484462.html), DeepSeekMoE paragraph:
+// the sqrt(softplus(.)) gate activation.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+#include <climits>
+
+namespace fp4moe {
+
+// ---------------------------------------------------------------------------
+// MXFP4 packing.  One thread per 8 consecutive K elements; four threads share
+// a 32-element block (scale X = floor(log2 amax) - 2, codes = RNE E2M1 of
+// w * 2^-X saturated to +-6, low nibble = even element).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) pack_fp4_kernel(const float *__restrict__ w, uint8_t *__restrict__ w_fp4,
+                                                       uint8_t *__restrict__ w_scale, long long n8)
+{
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool valid = gid < n8;
+    float v[8];
+    if (valid) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(w) + 2 * gid);
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(w) + 2 * gid + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; i++) v[i] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    int X = (amax == 0.f || ef == 0) ? -127 : ef - 127 - 2;
+    X = X < -127 ? -127 : X;
+    const float s = exp2i(-X);
+    uint32_t codes = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++) codes |= cvt_e2m1x2(v[2 * i] * s, v[2 * i + 1] * s) << (8 * i);
+    if (valid) {
+        reinterpret_cast<uint32_t *>(w_fp4)[gid] = codes;
+        if ((gid & 3) == 0) w_scale[gid >> 2] = (uint8_t)(X + 127);
+    }
+}
+
+cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, long long rows, int K,
+                            cudaStream_t st)
+{
+    const long long n8 = rows * (long long)(K / 8);
+    if (n8 == 0) return cudaSuccess;
+    const long long blocks = (n8 + 255) / 256;
+    pack_fp4_kernel<<<(unsigned)blocks, 256, 0, st>>>(w, w_fp4, w_scale, n8);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// FP8 quantisation of one 128-channel group of a bf16 row by one warp:
+// each lane handles 4 channels; returns the group's scale exponent e.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int quant_group_warp(const uint16_t *__restrict__ xg, uint8_t *__restrict__ qg)
+{
+    const int lane = threadIdx.x & 31;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(xg) + lane);
+    float v[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
+                  bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const int e = e4m3_scale_exp(amax);
+    const float s = exp2i(-e);
+    const uint32_t q = cvt_e4m3x2(v[0] * s, v[1] * s) | (cvt_e4m3x2(v[2] * s, v[3] * s) << 16);
+    reinterpret_cast<uint32_t *>(qg)[lane] = q;
+    return e;
+}
+
+__device__ __forceinline__ void quant_row_warp(const uint16_t *__restrict__ xrow, uint8_t *__restrict__ qrow,
+                                               uint8_t *__restrict__ srow, int d, int s_stride)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = d / 128;
+    for (int g = 0; g < G; g++) {
+        const int e = quant_group_warp(xrow + g * 128, qrow + g * 128);
+        if (lane == 0) srow[g] = (uint8_t)(e + 127);
+    }
+    for (int g = G + lane; g < s_stride; g += 32) srow[g] = 0;
+}
+
+__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
+                                                       uint8_t *__restrict__ xs, int xs_stride, int T, int d)
+{
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    quant_row_warp(x + (size_t)t * d, xq + (size_t)t * d, xs + (size_t)t * xs_stride, d, xs_stride);
+}
+
+cudaError_t launch_quantize(const uint16_t *x, uint8_t *xq, uint8_t *xs, int xs_stride, int T, int d,
+                            cudaStream_t st)
+{
+    if (T == 0) return cudaSuccess;
+    quantize_kernel<<<(T + 7) / 8, 256, 0, st>>>(x, xq, xs, xs_stride, T, d);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Gate logits in the fixed fp32 order: for each (t, e) and l = 0..31 a partial
+// sum over channels i = l, l+32, ... (increasing i, fused multiply-adds), then
+// a binary tree with offsets 16..1.  Here warp lane l IS partial sum l: a warp
+// owns a TW x EW tile of (token, expert) pairs, every lane accumulates its
+// channel subsequence for all of them, and the final xor-butterfly adds
+// exactly the tree's pairs (each add is commutative, so every lane ends with
+// the tree's total).  Chunks of 128 channels of x and gate_w are staged in
+// shared memory through a cp.async pipeline.
+// ---------------------------------------------------------------------------
+namespace gate {
+constexpr int CH = 128;
+constexpr int STAGES = 4;
+
+__device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, bool pred)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(pred ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_4_zfill(void *dst, const void *src, bool pred)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(pred ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+} // namespace gate
+
+template <int TW, int EW, int WT, int WE, bool VEC_W>
+__global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t *__restrict__ x,
+                                                                  const float *__restrict__ gate_w,
+                                                                  const float *__restrict__ bias,
+                                                                  float *__restrict__ z, int T, int d, int E)
+{
+    using namespace gate;
+    constexpr int NT = WT * WE * 32;
+    constexpr int CT = TW * WT;           // tokens per CTA
+    constexpr int CE = EW * WE;           // experts per CTA
+    constexpr int WROW = CE + 4;          // padded gate_w row in shared memory (floats)
+    constexpr int XROW = CH + 8;          // padded x row (bf16 elements)
+    static_assert(CE % 4 == 0, "expert tile must be a multiple of 4");
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint16_t *xs_ = reinterpret_cast<uint16_t *>(smem_raw);                       // [STAGES][CT][XROW]
+    float *ws_ = reinterpret_cast<float *>(smem_raw + STAGES * CT * XROW * 2);     // [STAGES][CH][WROW]
+
+    const int t0 = blockIdx.x * CT;
+    const int e0 = blockIdx.y * CE;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wt = warp / WE, we = warp % WE;
+    const int nch = d / CH;
+
+    auto load_chunk = [&](int c) {
+        if (c >= nch) return;
+        const int st = c % STAGES;
+        const int i0 = c * CH;
+        uint16_t *xd = xs_ + st * CT * XROW;
+        for (int q = threadIdx.x; q < CT * (CH / 8); q += NT) {
+            const int r = q / (CH / 8), c8 = q % (CH / 8);
+            const int t = t0 + r;
+            const bool ok = t < T;
+            cp_async_16_zfill(xd + r * XROW + c8 * 8, x + (size_t)(ok ? t : 0) * d + i0 + c8 * 8, ok);
+        }
+        float *wd = ws_ + st * CH * WROW;
+        if (VEC_W) {
+            for (int q = threadIdx.x; q < CH * (CE / 4); q += NT) {
+                const int r = q / (CE / 4), c4 = q % (CE / 4);
+                const int e = e0 + c4 * 4;
+                const bool ok = e < E;
+                cp_async_16_zfill(wd + r * WROW + c4 * 4, gate_w + (size_t)(i0 + r) * E + (ok ? e : 0), ok);
+            }
+        } else {
+            for (int q = threadIdx.x; q < CH * CE; q += NT) {
+                const int r = q / CE, c1 = q % CE;
+                const int e = e0 + c1;
+                const bool ok = e < E;
+                cp_async_4_zfill(wd + r * WROW + c1, gate_w + (size_t)(i0 + r) * E + (ok ? e : 0), ok);
+            }
+        }
+    };
+
+    float acc[TW][EW];
+#pragma unroll
+    for (int a = 0; a < TW; a++)
+#pragma unroll
+        for (int b = 0; b < EW; b++) acc[a][b] = 0.f;
+
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; s++) {
+        load_chunk(s);
+        cp_async_commit();
+    }
+    for (int c = 0; c < nch; c++) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        load_chunk(c + STAGES - 1);
+        cp_async_commit();
+        const int st = c % STAGES;
+        const uint16_t *xb = xs_ + st * CT * XROW + (wt * TW) * XROW;
+        const float *wb = ws_ + st * CH * WROW + we * EW;
+#pragma unroll
+        for (int q = 0; q < CH / 32; q++) {
+            const int i = q * 32 + lane;         // this lane's channel in the chunk
+            float xv[TW], wv[EW];
+#pragma unroll
+            for (int a = 0; a < TW; a++) xv[a] = bf16_bits_to_f32(xb[a * XROW + i]);
+#pragma unroll
+            for (int b = 0; b < EW; b += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(wb + i * WROW + b);
+                wv[b] = f.x; wv[b + 1] = f.y; wv[b + 2] = f.z; wv[b + 3] = f.w;
+            }
+#pragma unroll
+            for (int a = 0; a < TW; a++)
+#pragma unroll
+                for (int b = 0; b < EW; b++) acc[a][b] = fmaf(xv[a], wv[b], acc[a][b]);
+        }
+    }
+    cp_async_wait<0>();
+
+#pragma unroll
+    for (int a = 0; a < TW; a++)
+#pragma unroll
+        for (int b = 0; b < EW; b++) {
+            float v = acc[a][b];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, off);
+            acc[a][b] = v;
+        }
+    // every lane holds every total; lane (a*EW+b) % 32 writes pair (a, b)
+#pragma unroll
+    for (int a = 0; a < TW; a++)
+#pragma unroll
+        for (int b = 0; b < EW; b++) {
+            if (((a * EW + b) & 31) != lane) continue;
+            const int t = t0 + wt * TW + a, e = e0 + we * EW + b;
+            if (t < T && e < E) {
+                float v = acc[a][b];
+                if (bias) v = v + bias[e];
+                z[(size_t)t * E + e] = v;
+            }
+        }
+}
+
+template <int TW, int EW, int WT, int WE, bool VEC_W>
+static cudaError_t launch_gate_cfg(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T, int d,
+                                   int E, cudaStream_t st)
+{
+    constexpr int CT = TW * WT, CE = EW * WE;
+    const size_t smem = (size_t)gate::STAGES * (CT * (gate::CH + 8) * 2 + gate::CH * (CE + 4) * 4);
+    auto kern = gate_logits_kernel<TW, EW, WT, WE, VEC_W>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((T + CT - 1) / CT, (E + CE - 1) / CE);
+    kern<<<grid, WT * WE * 32, smem, st>>>(x, gate_w, bias, z, T, d, E);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T, int d,
+                               int E, cudaStream_t st)
+{
+    if (T == 0) return cudaSuccess;
+    const bool vec = (E % 4) == 0;
+    if (T >= 2048) {
+        return vec ? launch_gate_cfg<8, 16, 4, 2, true>(x, gate_w, bias, z, T, d, E, st)
+                   : launch_gate_cfg<8, 16, 4, 2, false>(x, gate_w, bias, z, T, d, E, st);
+    }
+    return vec ? launch_gate_cfg<4, 8, 4, 1, true>(x, gate_w, bias, z, T, d, E, st)
+               : launch_gate_cfg<4, 8, 4, 1, false>(x, gate_w, bias, z, T, d, E, st);
+}
+
+// ---------------------------------------------------------------------------
+// Top-k + weights, one warp per token.  Selection order: larger logit first,
+// equal logits -> lower expert index.  s_j = fp32(sqrt(softplus(z_j))) with
+// softplus(z) = max(z, 0) + log1p(exp(-|z|)) in double; w_j = s_j / S, S the
+// fp32 sum of s_j in slot order (w_j = 1/k when S == 0).  Optionally
+// quantises the token's x row in the same pass.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ z, int32_t *__restrict__ topk_idx,
+                                                   float *__restrict__ topk_w, const uint16_t *__restrict__ x,
+                                                   uint8_t *__restrict__ xq, uint8_t *__restrict__ xs, int xs_stride,
+                                                   int T, int d, int E, int k, unsigned *status)
+{
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    const float *zt = z + (size_t)t * E;
+    float v[8];
+    bool bad = false;
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+        const int e = lane + 32 * m;
+        float val = -INFINITY;
+        if (e < E) {
+            val = zt[e];
+            if (isnan(val)) {
+                bad = true;
+                val = -INFINITY;
+            }
+        }
+        v[m] = val;
+    }
+    uint32_t taken = 0;
+    float my_z = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < k; j++) {
+        float bz = -INFINITY;
+        int be = INT_MAX;
+#pragma unroll
+        for (int m = 0; m < 8; m++) {
+            const int e = lane + 32 * m;
+            if (e < E && !((taken >> m) & 1u) && (v[m] > bz || (v[m] == bz && e < be))) {
+                bz = v[m];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float oz = __shfl_xor_sync(0xffffffffu, bz, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (oz > bz || (oz == bz && oe < be)) {
+                bz = oz;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == j) {
+            my_z = bz;
+            my_e = be;
+        }
+    }
+    if (bad && lane == 0) flag_status(status, kStatusBadData);
+    float s = 0.f;
+    if (lane < k) {
+        const double zd = (double)my_z;
+        const double sp = (zd > 0.0 ? zd : 0.0) + log1p(exp(-fabs(zd)));
+        s = (float)sqrt(sp);
+    }
+    float S = 0.f;
+    for (int j = 0; j < k; j++) S = S + __shfl_sync(0xffffffffu, s, j);
+    if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = my_e;
+        topk_w[(size_t)t * k + lane] = (S == 0.f) ? 1.0f / (float)k : s / S;
+    }
+    if (xq) quant_row_warp(x + (size_t)t * d, xq + (size_t)t * d, xs + (size_t)t * xs_stride, d, xs_stride);
+}
+
+cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const uint16_t *x, uint8_t *xq,
+                        uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st)
+{
+    if (T == 0) return cudaSuccess;
+    topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(z, topk_idx, topk_w, x, xq, xs, xs_stride, T, d, E, k, status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch plan: one CTA of 32 warps; warp w owns a contiguous chunk of the
+// pairs.  Pass 1 counts experts per chunk (warp-private rows of a shared
+// table, no atomics); a scan turns the table into each chunk's first free
+// slot per expert; pass 2 walks the chunk again in order and places every
+// pair at (its chunk's slot) + (rank among equal experts before it in the
+// 32-pair step).  The result is the unique stable order.
+// ---------------------------------------------------------------------------
+constexpr int kPlanWarps = 32;
+
+__global__ void __launch_bounds__(kPlanWarps * 32) plan_kernel(const int32_t *__restrict__ topk_idx,
+                                                               int32_t *__restrict__ expert_offsets,
+                                                               int32_t *__restrict__ sorted_pair,
+                                                               int32_t *__restrict__ pair_pos,
+                                                               int32_t *__restrict__ tile_prefix, long long P, int E,
+                                                               unsigned *status)
+{
+    extern __shared__ int cnt[];                  // [kPlanWarps][E]
+    __shared__ int tot[257];
+    __shared__ int tiles[257];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+
+    const long long chunk = (P + kPlanWarps - 1) / kPlanWarps;
+    const long long pb = warp * chunk;
+    const long long pe = (pb + chunk < P) ? pb + chunk : P;
+    int *my = cnt + warp * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    bool bad = false;
+
+    for (long long base = pb; base < pe; base += 32) {
+        const long long p = base + lane;
+        const bool valid = p < pe;
+        int e = valid ? __ldg(topk_idx + p) : -1;
+        if (valid && (e < 0 || e >= E)) {
+            bad = true;
+            e = 0;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (valid && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+    }
+    __syncthreads();
+
+    // per-expert totals, then an exclusive scan over experts (warp 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int s = 0;
+        for (int w = 0; w < kPlanWarps; w++) s += cnt[w * E + e];
+        tot[e] = s;
+        tiles[e] = (s + kTileM - 1) / kTileM;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0, trun = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int c = e < E ? tot[e] : 0;
+            const int tc = e < E ? tiles[e] : 0;
+            int inc = c, tinc = tc;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, inc, off);
+                const int b = __shfl_up_sync(0xffffffffu, tinc, off);
+                if (lane >= off) {
+                    inc += a;
+                    tinc += b;
+                }
+            }
+            if (e < E) {
+                expert_offsets[e] = run + inc - c;
+                if (tile_prefix) tile_prefix[e] = trun + tinc - tc;
+                tot[e] = run + inc - c;          // becomes the expert's first slot
+            }
+            run += __shfl_sync(0xffffffffu, inc, 31);
+            trun += __shfl_sync(0xffffffffu, tinc, 31);
+        }
+        if (lane == 0) {
+            expert_offsets[E] = run;
+            if (tile_prefix) tile_prefix[E] = trun;
+        }
+    }
+    __syncthreads();
+    // chunk-local first slots
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = tot[e];
+        for (int w = 0; w < kPlanWarps; w++) {
+            const int c = cnt[w * E + e];
+            cnt[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+
+    for (long long base = pb; base < pe; base += 32) {
+        const long long p = base + lane;
+        const bool valid = p < pe;
+        int e = valid ? __ldg(topk_idx + p) : -1;
+        if (valid && (e < 0 || e >= E)) e = 0;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int pos = 0;
+        if (valid) pos = my[e] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+        if (valid) {
+            sorted_pair[pos] = (int32_t)p;
+            pair_pos[p] = pos;
+        }
+    }
+    if (bad) flag_status(status, kStatusBadData);
+}
+
+cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
+                        int32_t *tile_prefix, int T, int E, int k, unsigned *status, cudaStream_t st)
+{
+    const long long P = (long long)T * k;
+    const size_t smem = (size_t)kPlanWarps * E * sizeof(int);
+    cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    plan_kernel<<<1, kPlanWarps * 32, smem, st>>>(topk_idx, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E,
+                                                  status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch copy: row `pos` of the expert-ordered activations is the quantised
+// row of token sorted_pair[pos] / k (one warp per row, 16-byte vectors).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dispatch_kernel(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xs,
+                                                       int xs_stride, const int32_t *__restrict__ sorted_pair,
+                                                       uint8_t *__restrict__ xq_sorted, uint8_t *__restrict__ xs_sorted,
+                                                       long long P, int d, int k)
+{
+    const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (pos >= P) return;
+    const int lane = threadIdx.x & 31;
+    const int t = __ldg(sorted_pair + pos) / k;
+    const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)t * d);
+    uint4 *dst = reinterpret_cast<uint4 *>(xq_sorted + (size_t)pos * d);
+    for (int i = lane; i < d / 16; i += 32) dst[i] = __ldg(src + i);
+    const uint32_t *ss = reinterpret_cast<const uint32_t *>(xs + (size_t)t * xs_stride);
+    uint32_t *sd = reinterpret_cast<uint32_t *>(xs_sorted + (size_t)pos * xs_stride);
+    for (int i = lane; i < xs_stride / 4; i += 32) sd[i] = __ldg(ss + i);
+}
+
+cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride, const int32_t *sorted_pair,
+                            uint8_t *xq_sorted, uint8_t *xs_sorted, long long P, int d, int k, cudaStream_t st)
+{
+    if (P == 0) return cudaSuccess;
+    dispatch_kernel<<<(unsigned)((P + 7) / 8), 256, 0, st>>>(xq, xs, xs_stride, sorted_pair, xq_sorted, xs_sorted, P,
+                                                             d, k);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Combine: out[t][c] = bf16(acc), acc = fmaf(w_j, y_j[c], acc) over slots
+// j = 0..k-1 from acc = 0 -- a fixed order, no atomics.  One thread per
+// (token, 8 channels).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ y,
+                                                      const int32_t *__restrict__ pair_pos,
+                                                      const float *__restrict__ topk_w, uint16_t *__restrict__ out,
+                                                      int T, int d, int k)
+{
+    const int per_tok = d / 8;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (long long)T * per_tok) return;
+    const int t = (int)(gid / per_tok), c8 = (int)(gid % per_tok);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) acc[i] = 0.f;
+    for (int j = 0; j < k; j++) {
+        const float w = __ldg(topk_w + (size_t)t * k + j);
+        const int pos = __ldg(pair_pos + (size_t)t * k + j);
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(y + (size_t)pos * d) + c8);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            acc[2 * i] = fmaf(w, bf16_bits_to_f32(u[i] & 0xFFFFu), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(w, bf16_bits_to_f32(u[i] >> 16), acc[2 * i + 1]);
+        }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4 *>(out + (size_t)t * d)[c8] = o;
+}
+
+cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,
+                           int d, int k, cudaStream_t st)
+{
+    const long long n = (long long)T * (d / 8);
+    if (n == 0) return cudaSuccess;
+    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, pair_pos, topk_w, out, T, d, k);
+    return cudaGetLastError();
+}
+
+} // namespace fp4moe

@@ -1,0 +1,226 @@
+/*
+ * fp4moe.h -- C ABI of libfp4moe.so: the forward pass of an MoE layer with
+ * FP4 (E2M1) expert weights on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer ("DeepSeek-V4揭秘：细粒度专家并行隐藏通信时延，FP4量化与TileLang协同优化百万Token上下文",
+ * itsolotime.com/archives/32374, section 1.1: four stages -- dispatch,
+ * linear-1, linear-2, combine) is, for every token t:
+ *   z      = x_t . gate_w  (+ bias)                  fp32, fixed order (below)
+ *   S      = top-k experts by z                       ties -> lower expert index
+ *   w_j    = sqrt(softplus(z_j)) / sum_j sqrt(softplus(z_j))
+ *            (gate activation of "DeepSeek V4架构学习笔记", 67808.cn/a/484462.html,
+ *            DeepSeekMoE paragraph; renormalised to sum 1)
+ *   xq     = FP8 E4M3 of x_t, one power-of-two scale per 128 channels
+ *            (FP8 dispatch, section 1.4 of the first page)
+ *   h_e    = silu(xq W13_e[gate]^T) * (xq W13_e[up]^T)    -> FP8, scale per 128
+ *   y_e    = bf16(h_e W2_e^T)                          (BF16 combine payload)
+ *   out_t  = bf16( sum_j w_j * y_{e_j} )   fp32 fused multiply-adds in slot order
+ * with expert weights stored as MXFP4: E2M1 codes plus one UE8M0 power-of-two
+ * scale per 32 elements along K (section 4, "FP4 量化感知训练", of the first
+ * page; the FP4 -> FP8 step is exact, so the contraction runs on FP8 tensor
+ * cores with the 1x32 scales applied by the block-scaled MMA).
+ *
+ * Conventions for every function:
+ *  - Pointers marked "device" are caller-owned device memory; the library
+ *    never frees them and keeps no pointer after the call returns.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL =
+ *    legacy default stream).  No function synchronises the stream except
+ *    moe_get_device_status.
+ *  - Every argument is checked on the host before anything is launched; on an
+ *    argument error the outputs are left untouched and nothing is enqueued.
+ *  - Return value: MOE_OK or an error code; nothing throws across the ABI.
+ *    Asynchronous device errors surface as MOE_ERR_CUDA from a later call, or
+ *    through moe_get_device_status.
+ *  - Shapes: T >= 0 (T == 0 is a no-op that returns MOE_OK), d % 256 == 0
+ *    (d % 128 == 0 for moe_quantize_act / moe_route), inter % 128 == 0,
+ *    1 <= k <= 8, k <= E <= 256, T * k < 2^31.
+ *  - Alignment: every device pointer 16-byte aligned; packed weights 32-byte
+ *    aligned (the tensor-memory-access rule for packed 4-bit data).
+ *  - Results are deterministic: repeated calls give identical bits, and a
+ *    token's output bits do not depend on the other tokens in the batch.
+ */
+#ifndef FP4MOE_H
+#define FP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* NULL or misaligned pointer, negative size */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported set above */
+    MOE_ERR_CUDA = 3,               /* a CUDA runtime call failed */
+    MOE_ERR_WORKSPACE = 4,          /* workspace allocation failed or too small */
+    MOE_ERR_TIMEOUT = 5,            /* a kernel gave up waiting on a barrier */
+    MOE_ERR_UNSUPPORTED_DEVICE = 6, /* the current device is not sm_103 */
+    MOE_ERR_DEVICE_FAULT = 7        /* a kernel flagged bad data (e.g. expert id out of range) */
+} moe_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *moe_status_string(moe_status s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int moe_version(void);
+
+/*
+ * moe_pack_fp4 -- MXFP4 weight quantisation (first page, section 4).
+ *   w        device, fp32 [E][N][K] row-major (K contiguous)
+ *   w_fp4    device, uint8 [E][N][K/2]: two E2M1 codes per byte, the low
+ *            nibble holds the even K index
+ *   w_scale  device, uint8 [E][N][K/32]: UE8M0 byte X + 127 per 32 K-elements,
+ *            X = floor(log2(max |w| of the block)) - 2 (X = -127 for an all-zero
+ *            block), clamped to [-127, 127]; codes are the round-to-nearest-even
+ *            E2M1 of w * 2^-X saturated to +-6.
+ * For the layer: W13 is [E][2*inter][d] (rows 0..inter-1 = gate projection,
+ * inter..2*inter-1 = up projection), W2 is [E][d][inter].
+ * Requires K % 32 == 0, E, N >= 1.  Load-time operation, off the hot path.
+ */
+moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale,
+                        int E, int N, int K, void *stream);
+
+/*
+ * moe_quantize_act -- FP8 E4M3 activation quantisation (first page, section 1.4,
+ * "FP8 dispatch").  One power-of-two scale per token per 128 channels:
+ * e = the smallest integer with max|x| <= 448 * 2^e (e = 0 for an all-zero
+ * group), clamped to [-127, 127]; xq = round-to-nearest-even E4M3 of x * 2^-e.
+ *   x   device, bf16 bit patterns [T][d]
+ *   xq  device, uint8 E4M3 codes [T][d]
+ *   xs  device, uint8 [T][d/128], byte e + 127
+ * This is the quantisation the forward pass applies to x (same kernel).
+ */
+moe_status moe_quantize_act(const uint16_t *x, uint8_t *xq, uint8_t *xs,
+                            int T, int d, void *stream);
+
+/*
+ * moe_route -- gate and top-k ("DeepSeek V4架构学习笔记", DeepSeekMoE paragraph).
+ *   x          device, bf16 [T][d]
+ *   gate_w     device, fp32 [d][E]
+ *   gate_bias  device, fp32 [E] added to the logits, or NULL
+ *   topk_idx   device, int32 [T][k]: slot j holds the j-th largest logit's
+ *              expert (logits descending, ties to the lower expert index)
+ *   topk_w     device, fp32 [T][k]: w_j = s_j / sum_j s_j (fp32 sum in slot
+ *              order), s_j = fp32(sqrt(softplus(z_j))) evaluated in double;
+ *              w_j = 1/k if the sum is 0
+ * Logits use a fixed fp32 order so routing is exactly reproducible: for each
+ * (t, e), 32 partial sums over channels i = l, l+32, ... accumulated with fused
+ * multiply-adds in increasing i, then added as a binary tree with offsets
+ * 16, 8, 4, 2, 1 (partial[l] += partial[l + off]); the bias is added last.
+ * Inputs must be finite.  Allocates T*E*4 bytes of stream-ordered scratch.
+ */
+moe_status moe_route(const uint16_t *x, const float *gate_w, const float *gate_bias,
+                     int32_t *topk_idx, float *topk_w, int T, int d, int E, int k, void *stream);
+
+/*
+ * moe_dispatch_plan -- expert-contiguous layout of the P = T*k token-expert
+ * pairs (first page, section 1.1 "dispatch"; section 3.2: a fixed token order
+ * keeps results deterministic).  Pair p = t*k + j.
+ *   topk_idx        device, int32 [T][k], values in [0, E)
+ *   expert_offsets  device, int32 [E+1]: start of expert e's group; [E] = P
+ *   sorted_pair     device, int32 [P]: pairs by ascending expert, ascending p
+ *                   within an expert (a stable counting sort)
+ *   pair_pos        device, int32 [P]: inverse of sorted_pair
+ * An out-of-range expert index sets MOE_ERR_DEVICE_FAULT in the device status
+ * word (see moe_get_device_status) and the outputs are then unspecified.
+ */
+moe_status moe_dispatch_plan(const int32_t *topk_idx, int32_t *expert_offsets,
+                             int32_t *sorted_pair, int32_t *pair_pos,
+                             int T, int E, int k, void *stream);
+
+/*
+ * moe_forward -- the whole layer: gate + top-k, FP8 quantisation of x,
+ * dispatch plan, grouped GEMM1 (W13, fused SwiGLU and FP8 re-quantisation of
+ * h with one power-of-two scale per 128 channels), grouped GEMM2 (W2, output
+ * rounded to bf16) and the combine out_t = bf16(fp32 fused multiply-add chain
+ * over slots j = 0..k-1 of w_j * y_j).
+ *   x                  device, bf16 [T][d]
+ *   gate_w             device, fp32 [d][E]
+ *   w13_fp4, w13_scale device, moe_pack_fp4 output for W13 [E][2*inter][d]
+ *   w2_fp4,  w2_scale  device, moe_pack_fp4 output for W2 [E][d][inter]
+ *   out                device, bf16 [T][d]
+ * Workspace (moe_workspace_size bytes) is allocated stream-ordered on `stream`
+ * and released on it before return.
+ */
+moe_status moe_forward(const uint16_t *x, const float *gate_w,
+                       const uint8_t *w13_fp4, const uint8_t *w13_scale,
+                       const uint8_t *w2_fp4, const uint8_t *w2_scale,
+                       uint16_t *out, int T, int d, int inter, int E, int k, void *stream);
+
+/* Options of moe_forward_ex.  Zero-initialise and set what is needed. */
+typedef struct moe_forward_opts {
+    const float *gate_bias;    /* device fp32 [E] added to the logits, or NULL */
+    void *workspace;           /* device, >= moe_workspace_size bytes, 256-byte
+                                  aligned; NULL = allocate on the stream */
+    size_t workspace_bytes;
+    int32_t *topk_idx_out;     /* optional device copies of the routing: [T][k] */
+    float *topk_w_out;         /* [T][k] */
+    int32_t *pair_pos_out;     /* [T*k] position of pair t*k+j in expert order */
+    uint32_t flags;            /* must be 0 */
+    void **stage_events;       /* optional: MOE_STAGE_COUNT + 1 caller-created
+                                  cudaEvent_t, recorded on the stream before the
+                                  first stage, between stages and after the last
+                                  (per-stage timing); NULL = none */
+} moe_forward_opts;
+
+/* Stages of moe_forward_ex, in launch order (index into stage_events). */
+enum {
+    MOE_STAGE_GATE = 0,   /* fixed-order fp32 gate logits */
+    MOE_STAGE_TOPK,       /* top-k, weights and FP8 quantisation of x */
+    MOE_STAGE_PLAN,       /* dispatch plan (stable counting sort) */
+    MOE_STAGE_DISPATCH,   /* copy of every pair's FP8 token row into expert order */
+    MOE_STAGE_GEMM1,      /* grouped W13 GEMM + SwiGLU + FP8 re-quantisation */
+    MOE_STAGE_GEMM2,      /* grouped W2 GEMM, bf16 output */
+    MOE_STAGE_COMBINE,    /* slot-order weighted combine */
+    MOE_STAGE_COUNT
+};
+
+/* moe_forward with options (gate bias, caller workspace, routing outputs).
+ * With a caller workspace the call allocates nothing and can be captured in a
+ * CUDA graph. */
+moe_status moe_forward_ex(const uint16_t *x, const float *gate_w,
+                          const uint8_t *w13_fp4, const uint8_t *w13_scale,
+                          const uint8_t *w2_fp4, const uint8_t *w2_scale,
+                          uint16_t *out, int T, int d, int inter, int E, int k,
+                          void *stream, const moe_forward_opts *opts);
+
+/* Bytes of workspace moe_forward_ex needs for these shapes (0 for bad shapes). */
+size_t moe_workspace_size(int T, int d, int inter, int E, int k);
+
+/* Workspace regions, for inspecting intermediates in tests and tools.
+ * moe_workspace_layout writes the byte offset of each region into
+ * offsets[MOE_WS_COUNT] and its row stride in bytes into strides[MOE_WS_COUNT]
+ * (either may be NULL) and returns the total size (0 for bad shapes). */
+enum {
+    MOE_WS_XQ = 0,        /* uint8 E4M3 [T][d] */
+    MOE_WS_XS,            /* uint8 [T][stride], first d/128 bytes of a row used */
+    MOE_WS_LOGITS,        /* fp32 [T][E] */
+    MOE_WS_TOPK_IDX,      /* int32 [T][k] */
+    MOE_WS_TOPK_W,        /* fp32 [T][k] */
+    MOE_WS_EXPERT_OFFSETS,/* int32 [E+1] */
+    MOE_WS_SORTED_PAIR,   /* int32 [P] */
+    MOE_WS_PAIR_POS,      /* int32 [P] */
+    MOE_WS_TILE_PREFIX,   /* int32 [E+1] running count of 128-row tiles */
+    MOE_WS_HQ,            /* uint8 E4M3 [P][inter], rows in expert order */
+    MOE_WS_HS,            /* uint8 [P][stride], first inter/128 bytes used */
+    MOE_WS_Y,             /* bf16 [P][d], rows in expert order */
+    MOE_WS_XQ_SORTED,     /* uint8 E4M3 [P][d]: row p = xq of the pair's token, expert order */
+    MOE_WS_XS_SORTED,     /* uint8 [P][stride], scales of those rows */
+    MOE_WS_COUNT
+};
+size_t moe_workspace_layout(int T, int d, int inter, int E, int k,
+                            size_t *offsets, size_t *strides);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word: MOE_OK, MOE_ERR_TIMEOUT (a kernel gave up on a bounded wait) or
+ * MOE_ERR_DEVICE_FAULT (a kernel found bad data); MOE_ERR_CUDA if the
+ * synchronisation itself failed. */
+moe_status moe_get_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4MOE_H */

@@ -1,0 +1,341 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: MXFP4 packing, FP8 activation quantisation, routing indices, the
+dispatch plan.  Within the layer tolerance (max|err| <= 1e-2 max|ref|, per-token
+relative L2 <= 5e-3): the layer output.  Plus determinism (repeated calls give
+identical bits) and batch invariance (a token's output bits do not depend on
+the rest of the batch).  Every test here needs a GB300.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_expert_grouped_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+
+
+def capi():
+    from fp4_expert_grouped_gb300 import capi as c
+    return c
+
+
+def layer():
+    from fp4_expert_grouped_gb300 import layer as l
+    return l
+
+
+def f32(b):
+    return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_layer_tolerance(got_bits, ref_bits, what=""):
+    got, ref = f32(got_bits), f32(ref_bits)
+    err = np.abs(got - ref)
+    assert err.max() <= 1e-2 * np.abs(ref).max(), "%s max err %g vs max ref %g" % (what, err.max(), np.abs(ref).max())
+    rn = np.linalg.norm(ref, axis=-1)
+    en = np.linalg.norm(got - ref, axis=-1)
+    assert np.all(en[rn == 0] == 0), what
+    rel = en[rn > 0] / rn[rn > 0]
+    assert rel.max() <= 5e-3, "%s worst token rel L2 %g" % (what, rel.max())
+
+
+def small_case(T, d, inter, E, k, seed, bias=False):
+    w = inputs.Workload("case", T, d, inter, E, k, seed, zipf_bias=bias)
+    x, gw, b = inputs.make_x_gate(w, "cpu")
+    w13, w2 = inputs.make_all_experts(w, "cpu")
+    return w, x, gw, b, w13, w2
+
+
+def run_small_forward(w, x, gw, b, w13, w2):
+    pk = layer().pack_experts(w13.to(DEV), w2.to(DEV))
+    out, ti, tw, pp = layer().forward(x.to(DEV), gw.to(DEV), pk, w.k,
+                                      gate_bias=None if b is None else b.to(DEV), routing=True)
+    assert capi().moe_get_device_status() == 0
+    xb = inputs.bf16_bits(x)
+    f13, s13 = oracle.pack_fp4(w13.numpy())
+    f2, s2 = oracle.pack_fp4(w2.numpy())
+    assert np.array_equal(pk.w13_fp4.cpu().numpy(), f13) and np.array_equal(pk.w13_scale.cpu().numpy(), s13)
+    assert np.array_equal(pk.w2_fp4.cpu().numpy(), f2) and np.array_equal(pk.w2_scale.cpu().numpy(), s2)
+    ref, ridx, rw = oracle.moe_forward(xb, gw.numpy(), f13, s13, f2, s2, w.k, None if b is None else b.numpy())
+    assert np.array_equal(ti.cpu().numpy(), ridx)
+    assert np.allclose(tw.cpu().numpy(), rw, rtol=2e-7, atol=0)
+    offs, sp, ppos = oracle.dispatch_plan(ridx, w.E)
+    assert np.array_equal(pp.cpu().numpy(), ppos)
+    check_layer_tolerance(inputs.bf16_bits(out), ref)
+    return out, pk
+
+
+# --------------------------------------------------------------------------
+# bit-exact stages
+# --------------------------------------------------------------------------
+
+def test_pack_fp4_bitexact_special_values():
+    rng = np.random.default_rng(100)
+    E, N, K = 3, 40, 512
+    w = rng.normal(0, 0.03, (E, N, K)).astype(np.float32)
+    w[0, 0, :32] = 0.0
+    w[0, 1, :32] = -0.0
+    w[0, 2, :32] = np.float32(6.0 * 2.0 ** -7)
+    w[0, 2, 0] = np.float32(7.9 * 2.0 ** -7)
+    w[1, 3, 32:64] = np.float32(0.25 * 2.0 ** -5)
+    w[1, 3, 32] = np.float32(4.0 * 2.0 ** -5)
+    w[1, 4, :32] = np.float32(1e-40)                      # subnormal block
+    w[1, 5, :32] = rng.normal(0, 1e30, 32).astype(np.float32)
+    w[2, 6, :] = -np.abs(w[2, 6, :])
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    w[2, 7, :7] = mids
+    w[2, 7, 7] = 6.0
+    w[2, 8, :7] = -mids
+    w[2, 8, 7] = 6.0
+    wt = torch.from_numpy(w).to(DEV)
+    fp4 = torch.empty((E, N, K // 2), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((E, N, K // 32), dtype=torch.uint8, device=DEV)
+    capi().moe_pack_fp4(wt, fp4, sc)
+    of, os_ = oracle.pack_fp4(w)
+    assert np.array_equal(sc.cpu().numpy(), os_)
+    assert np.array_equal(fp4.cpu().numpy(), of)
+
+
+def test_quantize_act_bitexact():
+    rng = np.random.default_rng(101)
+    T, d = 37, 768
+    xf = rng.normal(0, 1, (T, d)).astype(np.float32)
+    xf[0, :128] = 0
+    xf[1, :] *= 1e-30
+    xf[2, 130] = 3e38
+    xf[3, :] = np.round(xf[3, :] * 4) / 4
+    x = torch.from_numpy(xf).to(torch.bfloat16)
+    xq = torch.empty((T, d), dtype=torch.uint8, device=DEV)
+    xs = torch.empty((T, d // 128), dtype=torch.uint8, device=DEV)
+    capi().moe_quantize_act(x.to(DEV), xq, xs)
+    oq, os_ = oracle.quant_act(inputs.bf16_bits(x))
+    assert np.array_equal(xs.cpu().numpy(), os_)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+
+
+@pytest.mark.parametrize("T,d,E,k,ties,bias", [
+    (32, 256, 8, 2, False, False),
+    (1, 512, 16, 4, False, False),
+    (128, 4096, 256, 8, False, False),
+    (200, 1024, 64, 8, True, False),
+    (64, 512, 8, 8, False, False),        # k == E
+    (96, 768, 256, 6, False, True),
+    (50, 384, 13, 3, True, True),         # E not a multiple of 4
+])
+def test_route_bitexact(T, d, E, k, ties, bias):
+    rng = np.random.default_rng(T * 31 + E)
+    x = torch.from_numpy(rng.normal(0, 1, (T, d)).astype(np.float32)).to(torch.bfloat16)
+    gw = (rng.normal(0, 1, (d, E)) / np.sqrt(d)).astype(np.float32)
+    if ties:
+        gw[:, E - 1] = gw[:, 0]
+        gw[:, 2] = gw[:, 1]
+    b = rng.normal(0, 1, E).astype(np.float32) if bias else None
+    ti = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    capi().moe_route(x.to(DEV), torch.from_numpy(gw).to(DEV), None if b is None else torch.from_numpy(b).to(DEV),
+                     ti, tw)
+    ridx, rw = oracle.route(inputs.bf16_bits(x), gw, k, b)
+    assert np.array_equal(ti.cpu().numpy(), ridx)
+    assert np.allclose(tw.cpu().numpy(), rw, rtol=2e-7, atol=0)
+    assert np.all(np.abs(tw.cpu().numpy().astype(np.float64).sum(1) - 1) <= k * 2.0 ** -24 + 1e-12)
+
+
+@pytest.mark.parametrize("T,E,k,skew", [(1, 8, 1, False), (33, 8, 2, False), (128, 256, 8, False),
+                                        (4096, 256, 8, True), (16384, 256, 8, False), (1000, 5, 5, False)])
+def test_dispatch_plan_bitexact(T, E, k, skew):
+    rng = np.random.default_rng(T + E)
+    if skew:
+        p = np.arange(1, E + 1, dtype=np.float64) ** -3.0
+        p /= p.sum()
+        idx = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    else:
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    sp = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    pp = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    capi().moe_dispatch_plan(torch.from_numpy(idx).to(DEV), offs, sp, pp, E)
+    ro, rs, rp = oracle.dispatch_plan(idx, E)
+    assert np.array_equal(offs.cpu().numpy(), ro)
+    assert np.array_equal(sp.cpu().numpy(), rs)
+    assert np.array_equal(pp.cpu().numpy(), rp)
+    assert capi().moe_get_device_status() == 0
+
+
+def test_dispatch_plan_flags_bad_expert_index():
+    idx = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32, device=DEV)
+    offs = torch.empty(5, dtype=torch.int32, device=DEV)
+    sp = torch.empty(4, dtype=torch.int32, device=DEV)
+    pp = torch.empty(4, dtype=torch.int32, device=DEV)
+    capi().moe_dispatch_plan(idx, offs, sp, pp, 4)
+    assert capi().moe_get_device_status() == 7          # MOE_ERR_DEVICE_FAULT
+    assert capi().moe_get_device_status() == 0          # read-and-clear
+
+
+# --------------------------------------------------------------------------
+# whole layer
+# --------------------------------------------------------------------------
+
+def test_forward_tiny_all_tokens():
+    w = inputs.WORKLOADS["tiny"]
+    x, gw, b = inputs.make_x_gate(w, "cpu")
+    w13, w2 = inputs.make_all_experts(w, "cpu")
+    run_small_forward(w, x, gw, b, w13, w2)
+
+
+@pytest.mark.parametrize("T,d,inter,E,k,bias", [
+    (1, 256, 128, 8, 2, False),          # single token
+    (300, 256, 128, 8, 2, False),        # ragged tiles: expert groups not a multiple of 128 rows
+    (257, 512, 384, 16, 4, True),        # several weight blocks and K stages, biased gate
+    (64, 768, 256, 4, 4, False),         # k == E
+])
+def test_forward_small_shapes(T, d, inter, E, k, bias):
+    w, x, gw, b, w13, w2 = small_case(T, d, inter, E, k, seed=T + d, bias=bias)
+    if bias:
+        b = torch.from_numpy(np.random.default_rng(T).normal(0, 1, E).astype(np.float32))
+    run_small_forward(w, x, gw, b, w13, w2)
+
+
+def test_forward_identical_experts_reduce_to_one():
+    """Every expert identical: each token's output equals the single-expert
+    layer's (E = 1, k = 1) within one bf16 ulp."""
+    w, x, gw, b, w13, w2 = small_case(48, 256, 128, 8, 3, seed=9)
+    w13 = w13[:1].repeat(8, 1, 1).contiguous()
+    w2 = w2[:1].repeat(8, 1, 1).contiguous()
+    pk = layer().pack_experts(w13.to(DEV), w2.to(DEV))
+    out = layer().forward(x.to(DEV), gw.to(DEV), pk, 3)
+    pk1 = layer().pack_experts(w13[:1].to(DEV), w2[:1].to(DEV))
+    one = layer().forward(x.to(DEV), gw[:, :1].contiguous().to(DEV), pk1, 1)
+    a, b1 = f32(inputs.bf16_bits(out)), f32(inputs.bf16_bits(one))
+    assert np.all(np.abs(a - b1) <= np.abs(b1) * 2.0 ** -7)
+
+
+def _sampled_oracle(w, x, gw, bias, tokens, pk_gpu):
+    """Oracle output rows for `tokens`; packs (with the oracle) only the experts
+    those tokens route to, and checks the GPU packs of those experts bit-exactly."""
+    xb = inputs.bf16_bits(x)
+    gwn = gw.cpu().numpy()
+    bn = None if bias is None else bias.cpu().numpy()
+    ridx, _ = oracle.route(xb[tokens], gwn, w.k, bn)
+    need = sorted(set(ridx.reshape(-1).tolist()))
+    f13 = np.zeros((w.E, 2 * w.inter, w.d // 2), np.uint8)
+    s13 = np.zeros((w.E, 2 * w.inter, w.d // 32), np.uint8)
+    f2 = np.zeros((w.E, w.d, w.inter // 2), np.uint8)
+    s2 = np.zeros((w.E, w.d, w.inter // 32), np.uint8)
+    for e in need:
+        a, b = inputs.make_expert(w, e, DEV)
+        f13[e], s13[e] = [v[0] for v in oracle.pack_fp4(a.cpu().numpy()[None])]
+        f2[e], s2[e] = [v[0] for v in oracle.pack_fp4(b.cpu().numpy()[None])]
+        assert np.array_equal(pk_gpu.w13_fp4[e].cpu().numpy(), f13[e])
+        assert np.array_equal(pk_gpu.w13_scale[e].cpu().numpy(), s13[e])
+        assert np.array_equal(pk_gpu.w2_fp4[e].cpu().numpy(), f2[e])
+        assert np.array_equal(pk_gpu.w2_scale[e].cpu().numpy(), s2[e])
+    ref, idx, wts = oracle.moe_forward(xb, gwn, f13, s13, f2, s2, w.k, bn, tokens=np.asarray(tokens, np.int32))
+    return ref, idx, wts
+
+
+@pytest.fixture(scope="module")
+def workload_cache():
+    return {}
+
+
+def _workload(name, cache):
+    if name not in cache:
+        cache.clear()
+        torch.cuda.empty_cache()
+        w = inputs.WORKLOADS[name]
+        x, gw, b = inputs.make_x_gate(w, DEV)
+        pk = layer().pack_workload(w, DEV)
+        cache[name] = (w, x, gw, b, pk)
+    return cache[name]
+
+
+@pytest.mark.parametrize("name", ["decode", "mid", "skew", "prefill"])
+def test_forward_full_size_sampled_tokens(name, workload_cache):
+    """Full-size workloads in the benchmark's launch configuration; the oracle
+    recomputes a seeded sample of tokens (every token is independent)."""
+    w, x, gw, b, pk = _workload(name, workload_cache)
+    out, ti, tw, pp = layer().forward(x, gw, pk, w.k, gate_bias=b, routing=True)
+    assert capi().moe_get_device_status() == 0
+    rng = np.random.default_rng(w.seed)
+    n = 6 if w.T > 4096 else 8
+    tokens = sorted(set([0, w.T - 1] + rng.choice(w.T, n, replace=False).tolist()))
+    ref, ridx, rw = _sampled_oracle(w, x, gw, b, tokens, pk)
+    assert np.array_equal(ti.cpu().numpy()[tokens], ridx)
+    check_layer_tolerance(inputs.bf16_bits(out)[tokens], ref, name)
+    # whole-batch properties checkable at any size: the plan is a bijection
+    ppn = pp.cpu().numpy()
+    assert np.array_equal(np.sort(ppn), np.arange(w.P))
+    # routing of every token against the oracle's (cheap: gate only)
+    if w.T <= 4096:
+        oi, _ = oracle.route(inputs.bf16_bits(x), gw.cpu().numpy(), w.k, None if b is None else b.cpu().numpy())
+        assert np.array_equal(ti.cpu().numpy(), oi)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_determinism_and_batch_invariance(name, workload_cache):
+    if name == "tiny":
+        w = inputs.WORKLOADS["tiny"]
+        x, gw, b = inputs.make_x_gate(w, DEV)
+        w13, w2 = inputs.make_all_experts(w, DEV)
+        pk = layer().pack_experts(w13, w2)
+    else:
+        w, x, gw, b, pk = _workload(name, workload_cache)
+    full = layer().forward(x, gw, pk, w.k, gate_bias=b)
+    for _ in range(5):
+        again = layer().forward(x, gw, pk, w.k, gate_bias=b)
+        assert torch.equal(full.view(torch.int16), again.view(torch.int16))
+    fb = full.view(torch.int16)
+    rng = np.random.default_rng(7)
+    for t in rng.choice(w.T, 8, replace=False).tolist() + [0, w.T - 1]:
+        alone = layer().forward(x[t:t + 1].contiguous(), gw, pk, w.k, gate_bias=b)
+        assert torch.equal(alone.view(torch.int16)[0], fb[t]), "token %d alone differs" % t
+    half = w.T // 2
+    for sl in (slice(0, half), slice(half, w.T), slice(3, w.T - 5)):
+        part = layer().forward(x[sl].contiguous(), gw, pk, w.k, gate_bias=b)
+        assert torch.equal(part.view(torch.int16), fb[sl])
+    perm = torch.from_numpy(rng.permutation(w.T)).to(DEV)
+    shuf = layer().forward(x[perm].contiguous(), gw, pk, w.k, gate_bias=b)
+    assert torch.equal(shuf.view(torch.int16), fb[perm])
+    assert capi().moe_get_device_status() == 0
+
+
+def test_workspace_intermediates_tiny():
+    """xq/xs in the workspace bit-exact; h (dequantised hq) close to the oracle's."""
+    w = inputs.WORKLOADS["tiny"]
+    x, gw, _ = inputs.make_x_gate(w, "cpu")
+    w13, w2 = inputs.make_all_experts(w, "cpu")
+    pk = layer().pack_experts(w13.to(DEV), w2.to(DEV))
+    ws = layer().workspace(w.T, w.d, w.inter, w.E, w.k)
+    layer().forward(x.to(DEV), gw.to(DEV), pk, w.k, ws=ws)
+    total, off, st = capi().moe_workspace_layout(w.T, w.d, w.inter, w.E, w.k)
+    wsn = ws.cpu().numpy()
+    xb = inputs.bf16_bits(x)
+    oq, os_ = oracle.quant_act(xb)
+    c = capi()
+    assert np.array_equal(wsn[off[c.MOE_WS_XQ]:][:w.T * w.d].reshape(w.T, w.d), oq)
+    xs = wsn[off[c.MOE_WS_XS]:][:w.T * st[c.MOE_WS_XS]].reshape(w.T, -1)[:, :w.d // 128]
+    assert np.array_equal(xs, os_)
+    ridx, _ = oracle.route(xb, gw.numpy(), w.k)
+    offs, sp, _ = oracle.dispatch_plan(ridx, w.E)
+    f13, s13 = oracle.pack_fp4(w13.numpy())
+    f2, s2 = oracle.pack_fp4(w2.numpy())
+    hq = wsn[off[c.MOE_WS_HQ]:][:w.P * w.inter].reshape(w.P, w.inter)
+    hs = wsn[off[c.MOE_WS_HS]:][:w.P * st[c.MOE_WS_HS]].reshape(w.P, -1)[:, :w.inter // 128]
+    deq = torch.from_numpy(hq.copy()).view(torch.float8_e4m3fn).double().numpy().reshape(w.P, -1, 128)
+    deq = (deq * np.exp2(hs.astype(np.float64) - 127)[..., None]).reshape(w.P, -1)
+    for pos in range(w.P):
+        t, j = divmod(int(sp[pos]), w.k)
+        h, _, _, _ = oracle.expert_pair(oq[t], os_[t], ridx[t, j], f13, s13, f2, s2)
+        assert np.linalg.norm(deq[pos] - h) <= 0.05 * np.linalg.norm(h) + 1e-30
