@@ -57,7 +57,11 @@ constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SFA_COL = 256;
 constexpr uint32_t SFB_COL = 264;
 constexpr uint32_t FULL_ARRIVALS = 1 + 32;     // expect_tx arrival + one cp.async arrival per producer lane
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE;
+// Transaction bytes per stage.  The copy of packed 4-bit data spreads every
+// 8-byte group of 16 codes over a 16-byte slot (codes in the low 8 bytes, the
+// high 8 bytes left as they were), but the barrier's transaction count
+// advances by the packed bytes: half the shared-memory footprint of B.
+constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE / 2;
 
 // Instruction descriptor of the block-scaled MMA: A = E4M3 (format 0),
 // B = E2M1 (format 5), both K-major, N = 256, M = 128, UE8M0 scales.
