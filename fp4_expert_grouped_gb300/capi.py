@@ -31,7 +31,7 @@ STAGES = ["gate", "topk", "plan", "dispatch", "gemm1", "gemm2", "combine"]
 
 # every symbol the header declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_quantize_act", "moe_route",
-           "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
+           "moe_route_noalloc", "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
            "moe_workspace_layout", "moe_get_device_status"]
 
 
@@ -53,6 +53,8 @@ _lib.moe_quantize_act.argtypes = [_vp, _vp, _vp, _i, _i, _vp]
 _lib.moe_quantize_act.restype = _i
 _lib.moe_route.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.moe_route.restype = _i
+_lib.moe_route_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+_lib.moe_route_noalloc.restype = _i
 _lib.moe_dispatch_plan.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]
 _lib.moe_dispatch_plan.restype = _i
 _lib.moe_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
@@ -124,6 +126,16 @@ def moe_route(x, gate_w, gate_bias, topk_idx, topk_w, stream=None):
     k = topk_idx.shape[1]
     _check(_lib.moe_route(_ptr(x), _ptr(gate_w), _ptr(gate_bias), _ptr(topk_idx), _ptr(topk_w),
                           T, d, E, k, _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(x, gate_w, gate_bias, topk_idx, topk_w, stream=None):
+    """moe_route whose logits scratch is the library's fixed device array
+    (nothing is allocated; T * E <= 1048576; overlapping calls race)."""
+    T, d = x.shape
+    E = gate_w.shape[1]
+    k = topk_idx.shape[1]
+    _check(_lib.moe_route_noalloc(_ptr(x), _ptr(gate_w), _ptr(gate_bias), _ptr(topk_idx), _ptr(topk_w),
+                                  T, d, E, k, _stream(stream)), "moe_route_noalloc")
 
 
 def moe_dispatch_plan(topk_idx, expert_offsets, sorted_pair, pair_pos, E, stream=None):

@@ -84,6 +84,16 @@ bool layer_shape_ok(int T, int d, int inter, int E, int k)
 
 } // namespace
 
+moe_status device_query(int *num_sms, unsigned **status)
+{
+    DeviceInfo *di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    *num_sms = di->num_sms;
+    *status = di->status;
+    return MOE_OK;
+}
+
 bool workspace_layout(const Shapes &s, Workspace *ws)
 {
     if (!layer_shape_ok(s.T, s.d, s.inter, s.E, s.k)) return false;

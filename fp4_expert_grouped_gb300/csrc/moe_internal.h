@@ -6,7 +6,13 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "fp4moe.h"
+
 namespace fp4moe {
+
+// SM count and device address of the status word of the current device
+// (MOE_ERR_UNSUPPORTED_DEVICE unless it is an sm_103 part).
+moe_status device_query(int *num_sms, unsigned **status);
 
 // Tile sizes of the grouped GEMM (fixed for every batch size, so a token's
 // result never depends on how many other tokens share its expert).

@@ -115,6 +115,25 @@ moe_status moe_route(const uint16_t *x, const float *gate_w, const float *gate_b
                      int32_t *topk_idx, float *topk_w, int T, int d, int E, int k, void *stream);
 
 /*
+ * moe_route_noalloc -- moe_route for callers that cannot allocate device
+ * memory at call time (a serving loop whose allocator already owns all free
+ * device memory, a latency-critical loop that forbids allocator calls after
+ * start-up, a host program that does not let libraries call cudaMalloc).
+ * Same arguments, results and checks as moe_route; the pages describe
+ * nothing of the kind (it exists only for such callers).
+ * Its T*E fp32 logits live in a fixed 4 MiB array of device memory that
+ * every device loading the library holds until the process exits; the call
+ * allocates nothing.  Limit: T * E <= 1048576 (e.g. 4096 tokens with 256
+ * experts); larger shapes return MOE_ERR_WORKSPACE without launching.
+ * The first call on a device looks up that array's device address (once per
+ * device, with the device current); make that first call before any stream
+ * capture.  All calls share the array: calls that overlap on the GPU (e.g.
+ * on two streams at once) race and must be serialised by the caller.
+ */
+moe_status moe_route_noalloc(const uint16_t *x, const float *gate_w, const float *gate_bias,
+                             int32_t *topk_idx, float *topk_w, int T, int d, int E, int k, void *stream);
+
+/*
  * moe_dispatch_plan -- expert-contiguous layout of the P = T*k token-expert
  * pairs (first page, section 1.1 "dispatch"; section 3.2: a fixed token order
  * keeps results deterministic).  Pair p = t*k + j.
