@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (a smaller case of the workload, e.g. for an ncu capture)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (a smaller case of the workload, e.g. for an ncu capture)")
     return ap.parse_args()
 
 
@@ -399,6 +403,11 @@ def main():
     args = parse()
     from fp4_expert_grouped_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
+    if args.tokens or args.experts:
+        import dataclasses
+        T = args.tokens or w.T
+        E = args.experts or w.E
+        w = dataclasses.replace(w, name="%s[T=%d,E=%d]" % (w.name, T, E), T=T, E=E)
     world, rank, local = dist_setup(want_nccl=(args.impl == "ours"))
     if args.impl == "reference":
         run_reference(args, w, world, rank)

@@ -26,8 +26,8 @@ STATUS_NAMES = {
 }
 STAGES = ["gate", "topk", "plan", "dispatch", "gemm1", "gemm2", "combine"]
 (MOE_WS_XQ, MOE_WS_XS, MOE_WS_LOGITS, MOE_WS_TOPK_IDX, MOE_WS_TOPK_W, MOE_WS_EXPERT_OFFSETS,
- MOE_WS_SORTED_PAIR, MOE_WS_PAIR_POS, MOE_WS_TILE_PREFIX, MOE_WS_HQ, MOE_WS_HS, MOE_WS_Y,
- MOE_WS_XQ_SORTED, MOE_WS_XS_SORTED, MOE_WS_COUNT) = range(15)
+ MOE_WS_SORTED_PAIR, MOE_WS_PAIR_POS, MOE_WS_TILE_PREFIX, MOE_WS_HQ, MOE_WS_HS_TILES, MOE_WS_Y,
+ MOE_WS_XQ_SORTED, MOE_WS_XS_TILES, MOE_WS_COUNT) = range(15)
 
 # every symbol the header declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_quantize_act", "moe_route",
@@ -110,7 +110,8 @@ def moe_version():
 
 
 def moe_pack_fp4(w, w_fp4, w_scale, stream=None):
-    """w fp32 [E, N, K] -> w_fp4 uint8 [E, N, K/2], w_scale uint8 [E, N, K/32] (device tensors)."""
+    """w fp32 [E, N, K] -> tiled MXFP4: w_fp4 (E*N*K/2 bytes), w_scale (E*N*K/32 bytes),
+    device tensors of any shape with that many bytes (see include/fp4moe.h)."""
     E, N, K = w.shape if w.dim() == 3 else (1, *w.shape)
     _check(_lib.moe_pack_fp4(_ptr(w), _ptr(w_fp4), _ptr(w_scale), E, N, K, _stream(stream)), "moe_pack_fp4")
 

@@ -99,7 +99,9 @@ bool workspace_layout(const Shapes &s, Workspace *ws)
     if (!layer_shape_ok(s.T, s.d, s.inter, s.E, s.k)) return false;
     const size_t T = s.T, d = s.d, I = s.inter, E = s.E, k = s.k, P = T * k;
     const size_t xs_stride = scale_row_stride(s.d);
-    const size_t hs_stride = scale_row_stride(s.inter);
+    const size_t tiles = (size_t)max_row_tiles((long long)P, s.E);
+    const size_t xs_tiles = tiles * stage_groups(s.d) * kBlockScaleBytes;
+    const size_t hs_tiles = tiles * stage_groups(s.inter) * kBlockScaleBytes;
     size_t bytes[MOE_WS_COUNT], stride[MOE_WS_COUNT];
     bytes[MOE_WS_XQ] = T * d;                stride[MOE_WS_XQ] = d;
     bytes[MOE_WS_XS] = T * xs_stride;        stride[MOE_WS_XS] = xs_stride;
@@ -111,10 +113,10 @@ bool workspace_layout(const Shapes &s, Workspace *ws)
     bytes[MOE_WS_PAIR_POS] = P * 4;          stride[MOE_WS_PAIR_POS] = 4;
     bytes[MOE_WS_TILE_PREFIX] = (E + 1) * 4; stride[MOE_WS_TILE_PREFIX] = 4;
     bytes[MOE_WS_HQ] = P * I;                stride[MOE_WS_HQ] = I;
-    bytes[MOE_WS_HS] = P * hs_stride;        stride[MOE_WS_HS] = hs_stride;
+    bytes[MOE_WS_HS_TILES] = hs_tiles;       stride[MOE_WS_HS_TILES] = stage_groups(s.inter) * kBlockScaleBytes;
     bytes[MOE_WS_Y] = P * d * 2;             stride[MOE_WS_Y] = d * 2;
     bytes[MOE_WS_XQ_SORTED] = P * d;         stride[MOE_WS_XQ_SORTED] = d;
-    bytes[MOE_WS_XS_SORTED] = P * xs_stride; stride[MOE_WS_XS_SORTED] = xs_stride;
+    bytes[MOE_WS_XS_TILES] = xs_tiles;       stride[MOE_WS_XS_TILES] = stage_groups(s.d) * kBlockScaleBytes;
     size_t off = 0;
     for (int i = 0; i < MOE_WS_COUNT; i++) {
         ws->off[i] = off;
@@ -153,12 +155,12 @@ moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E,
     if (!w || !w_fp4 || !w_scale) return MOE_ERR_INVALID_ARG;
     if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
     if (!aligned(w, 16) || !aligned(w_fp4, 16) || !aligned(w_scale, 16)) return MOE_ERR_INVALID_ARG;
-    if (K % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (K % 128 || N % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((long long)E * N * K == 0) return MOE_OK;
     DeviceInfo *di;
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
-    return cuda_status(launch_pack_fp4(w, w_fp4, w_scale, (long long)E * N, K, (cudaStream_t)stream));
+    return cuda_status(launch_pack_fp4(w, w_fp4, w_scale, E, N, K, (cudaStream_t)stream));
 }
 
 moe_status moe_quantize_act(const uint16_t *x, uint8_t *xq, uint8_t *xs, int T, int d, void *stream)
@@ -272,11 +274,10 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     int32_t *sorted_pair = reinterpret_cast<int32_t *>(at(MOE_WS_SORTED_PAIR));
     int32_t *pair_pos = reinterpret_cast<int32_t *>(at(MOE_WS_PAIR_POS));
     int32_t *tile_prefix = reinterpret_cast<int32_t *>(at(MOE_WS_TILE_PREFIX));
-    uint8_t *hq = at(MOE_WS_HQ), *hs = at(MOE_WS_HS);
+    uint8_t *hq = at(MOE_WS_HQ), *hs_tiles = at(MOE_WS_HS_TILES);
     uint16_t *y = reinterpret_cast<uint16_t *>(at(MOE_WS_Y));
-    uint8_t *xq_sorted = at(MOE_WS_XQ_SORTED), *xs_sorted = at(MOE_WS_XS_SORTED);
+    uint8_t *xq_sorted = at(MOE_WS_XQ_SORTED), *xs_tiles = at(MOE_WS_XS_TILES);
     const int xs_stride = (int)ws.stride[MOE_WS_XS];
-    const int hs_stride = (int)ws.stride[MOE_WS_HS];
     const long long P = (long long)T * k;
 
     cudaError_t e = cudaSuccess;
@@ -293,7 +294,8 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
         e = launch_plan(topk_idx, offs, sorted_pair, pair_pos, tile_prefix, T, E, k, di->status, s);
     mark(MOE_STAGE_DISPATCH);
     if (e == cudaSuccess)
-        e = launch_dispatch(xq, xs, xs_stride, sorted_pair, xq_sorted, xs_sorted, P, d, k, s);
+        e = launch_dispatch(xq, xs, xs_stride, sorted_pair, topk_idx, offs, tile_prefix, xq_sorted, xs_tiles, P, d,
+                            k, s);
     mark(MOE_STAGE_GEMM1);
     GemmArgs g;
     std::memset(&g, 0, sizeof g);
@@ -306,22 +308,19 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     g.num_sms = di->num_sms;
     if (e == cudaSuccess) {
         g.a = xq_sorted;
-        g.a_scale = xs_sorted;
-        g.a_scale_stride = xs_stride;
+        g.a_scale_tiles = xs_tiles;
         g.b = w13_fp4;
         g.b_scale = w13_scale;
         g.N = 2 * inter;
         g.K = d;
         g.hq = hq;
-        g.hs = hs;
-        g.hs_stride = hs_stride;
+        g.hs_tiles = hs_tiles;
         e = launch_gemm1(g, inter, s);
     }
     mark(MOE_STAGE_GEMM2);
     if (e == cudaSuccess) {
         g.a = hq;
-        g.a_scale = hs;
-        g.a_scale_stride = hs_stride;
+        g.a_scale_tiles = hs_tiles;
         g.b = w2_fp4;
         g.b_scale = w2_scale;
         g.N = d;

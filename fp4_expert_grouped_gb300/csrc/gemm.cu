@@ -15,14 +15,19 @@
 // blocks are shared through L2, and the TMA loads of the next tiles run while
 // the current tile's MMAs execute.
 //
-// Warp roles (192 threads):
-//   warp 0      producer: TMA tile loads of A (pair rows, E4M3) and B (weights,
-//               E2M1 spread to one byte per code by the copy engine) plus
-//               4-byte cp.async copies of the scale factors, into a 4-stage ring
+// Warp roles (320 threads):
+//   warp 0      producer: TMA tile loads of A (pair rows, E4M3; only the
+//               16-row boxes holding valid rows when a tile is sparsely
+//               filled) and B (weights, E2M1 spread to one byte per code by the
+//               copy engine; the weights are stored in contiguous 8 KB blocks)
+//               and 512-byte bulk copies of scale factors stored in the
+//               tensor cores' scale-factor order, into a 4-stage ring
 //   warp 1      tensor-memory owner and MMA issuer (one elected thread):
 //               scale factors -> tensor memory (tcgen05.cp), then 4 MMAs of
 //               K = 32 per stage into a 128 x 256 fp32 accumulator
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, then
+//   warps 2-9   epilogue, two warps per 32-lane quarter of tensor memory, each
+//               with half of the columns: tcgen05.ld to registers, release of
+//               the accumulator to the MMA warp, then
 //               GEMM1: h = silu(g) * u, FP8 re-quantisation per 128 channels
 //               GEMM2: rounding to bf16
 // Every wait is bounded; on a timeout the CTA flags the status word and exits.
@@ -39,29 +44,33 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK;          // 16 KB of E4M3
 constexpr int B_STAGE = BN * BK;          // 32 KB: 256 rows x 128 codes, one byte per code in shared memory
 constexpr int B_HALF = B_STAGE / 2;
+constexpr int A_SMALL_ROWS = 16;          // row box used when a tile holds <= SMALL_TILE_ROWS valid rows
+constexpr int SMALL_TILE_ROWS = 64;
 constexpr int SFA_STAGE = 512;            // 128 rows x 4 bytes
 constexpr int SFB_STAGE = 1024;           // 256 rows x 4 bytes
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
-constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
+constexpr int OFF_AMAX = OFF_SFB + STAGES * SFB_STAGE;          // [2 tile parities][2 halves][128 rows] fp32
+constexpr int OFF_BAR = OFF_AMAX + 2 * 2 * BM * 4;
+constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2 + 4) * 8;   // + one amax-exchange barrier per lane quarter
 constexpr int OFF_PLAN = OFF_MISC + 16;
 constexpr int PLAN_INTS = 260;
 constexpr int SMEM_USED = OFF_PLAN + 2 * PLAN_INTS * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;                   // two warps per 32-lane quarter of tensor memory
+constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SFA_COL = 256;
 constexpr uint32_t SFB_COL = 264;
-constexpr uint32_t FULL_ARRIVALS = 1 + 32;     // expect_tx arrival + one cp.async arrival per producer lane
-// Transaction bytes per stage.  The copy of packed 4-bit data spreads every
-// 8-byte group of 16 codes over a 16-byte slot (codes in the low 8 bytes, the
-// high 8 bytes left as they were), but the barrier's transaction count
-// advances by the packed bytes: half the shared-memory footprint of B.
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE / 2;
+constexpr uint32_t FULL_ARRIVALS = 1;          // the producer's expect_tx arrival; the rest is transaction bytes
+// Transaction bytes of B per stage.  The copy of packed 4-bit data spreads
+// every 8-byte group of 16 codes over a 16-byte slot (codes in the low 8
+// bytes, the high 8 bytes left as they were), but the barrier's transaction
+// count advances by the packed bytes: half the shared-memory footprint.
+constexpr uint32_t B_STAGE_TX = B_STAGE / 2;
 
 // Instruction descriptor of the block-scaled MMA: A = E4M3 (format 0),
 // B = E2M1 (format 5), both K-major, N = 256, M = 128, UE8M0 scales.
@@ -71,7 +80,7 @@ constexpr uint32_t IDESC_BASE = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) <<
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Tile {
-    int e, n_block, row0, valid;
+    int e, m_tile, n_block, row0, valid;   // m_tile: index of the 128-row tile among all experts' tiles
 };
 
 __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, const int *s_offs, int E, int nb)
@@ -87,6 +96,7 @@ __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, con
     const int mb = s_tp[lo + 1] - s_tp[lo];
     const long long local = tile - (long long)s_tp[lo] * nb;
     const int m_block = (int)(local % mb);
+    t.m_tile = s_tp[lo] + m_block;
     t.n_block = (int)(local / mb);
     t.row0 = s_offs[lo] + m_block * BM;
     const int rem = s_offs[lo + 1] - t.row0;
@@ -96,8 +106,8 @@ __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, con
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmArgs g, const int out_dim)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA16,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs g, const int out_dim)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -105,10 +115,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = full + 2 * STAGES;
     uint64_t *acc_empty = acc_full + 1;
+    uint64_t *xbar = acc_empty + 1;            // [4] amax exchange of the two epilogue warps of a lane quarter
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
     int *s_offs = reinterpret_cast<int *>(smem + OFF_PLAN);
     int *s_tp = s_offs + PLAN_INTS;
+    float *s_amax = reinterpret_cast<float *>(smem + OFF_AMAX);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -124,12 +136,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 128);
+        mbar_init(acc_empty, EPI_WARPS * 32);
+        for (int i = 0; i < 4; i++) mbar_init(&xbar[i], 64);
         *abort_flag = 0;
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmA16);
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
@@ -148,60 +162,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        uint32_t stage = 0, phase = 0;
-        const uint32_t sfa_base = OFF_SFA, sfb_base = OFF_SFB;
-        for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-            const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb);
-            int rb0, rb1;
-            if (MODE == 1) {
-                rb0 = ti.n_block * 128;
-                rb1 = out_dim + ti.n_block * 128;
-            } else {
-                rb0 = ti.n_block * BN;
-                rb1 = rb0 + 128;
-            }
-            const uint8_t *arow[4];
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int r = lane + 32 * j;
-                arow[j] = g.a_scale + (size_t)(ti.row0 + (r < ti.valid ? r : 0)) * g.a_scale_stride;
-            }
-            const uint8_t *brow[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int r = lane + 32 * (j & 3);
-                const int wrow = (j < 4 ? rb0 : rb1) + r;
-                brow[j] = g.b_scale + ((size_t)ti.e * g.N + wrow) * (size_t)(g.K / 32);
-            }
-            for (int ks = 0; ks < nk; ks++) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
-                    *abort_flag = 1;
-                    break;
+        // One thread issues everything: per stage one or a few TMA row boxes
+        // of A, two 8 KB blocks of B codes (spread to one byte per code in
+        // shared memory by the 4-bit copy), and three 512-byte bulk copies of
+        // scale factors already in the tensor-core order.  (Prefetching B into
+        // L2 ahead of the ring was measured and made every workload slower.)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            const int nkt = g.K / 128;                         // K blocks per weight row block
+            const int ga = stage_groups(g.K);                   // activation scale groups per tile
+            // Where the B blocks of a tile start (first K block of each 128-row half).
+            auto b_blocks = [&](const Tile &t, long long &b0, long long &b1) {
+                int rb0, rb1;
+                if (MODE == 1) {
+                    rb0 = t.n_block * 128;
+                    rb1 = out_dim + t.n_block * 128;
+                } else {
+                    rb0 = t.n_block * BN;
+                    rb1 = rb0 + 128;
                 }
-                uint8_t *sa = smem + OFF_A + stage * A_STAGE;
-                uint8_t *sb = smem + OFF_B + stage * B_STAGE;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-                    tma_load_2d(sa, &tmA, &full[stage], ks * BK, ti.row0);
-                    tma_load_3d(sb, &tmB, &full[stage], ks * BK, rb0, ti.e);
-                    tma_load_3d(sb + B_HALF, &tmB, &full[stage], ks * BK, rb1, ti.e);
-                }
-                // scale words, written straight into the layout tcgen05.cp
-                // expects: row r of a 128-row block -> word (r % 32) * 4 + r / 32
-                uint8_t *sfa = smem + sfa_base + stage * SFA_STAGE;
-                uint8_t *sfb = smem + sfb_base + stage * SFB_STAGE;
-#pragma unroll
-                for (int j = 0; j < 4; j++) cp_async_4(sfa + (lane * 4 + j) * 4, arow[j] + 4 * (ks >> 2));
-#pragma unroll
-                for (int j = 0; j < 8; j++)
-                    cp_async_4(sfb + (j >> 2) * 512 + (lane * 4 + (j & 3)) * 4, brow[j] + 4 * ks);
-                cp_async_arrive_noinc(&full[stage]);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                b0 = ((long long)t.e * (g.N / 128) + rb0 / 128) * nkt;
+                b1 = ((long long)t.e * (g.N / 128) + rb1 / 128) * nkt;
+            };
+            long long tile = blockIdx.x;
+            Tile ti;
+            long long blk0 = 0, blk1 = 0;
+            for (; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+                ti = decode_tile(tile, s_tp, s_offs, E, nb);
+                b_blocks(ti, blk0, blk1);
+                // sparsely filled tiles (few rows of an expert) load only the
+                // 16-row boxes that hold valid rows
+                const bool small = ti.valid <= SMALL_TILE_ROWS;
+                const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
+                const uint32_t stage_tx =
+                    (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE) + B_STAGE_TX + SFA_STAGE + SFB_STAGE;
+                const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
+                for (int ks = 0; ks < nk; ks++) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    uint8_t *sa = smem + OFF_A + stage * A_STAGE;
+                    uint8_t *sb = smem + OFF_B + stage * B_STAGE;
+                    uint64_t *fb = &full[stage];
+                    mbar_arrive_expect_tx(fb, stage_tx);
+                    if (small) {
+                        for (int b = 0; b < a_boxes; b++)
+                            tma_load_2d(sa + b * A_SMALL_ROWS * BK, &tmA16, fb, ks * BK, ti.row0 + b * A_SMALL_ROWS);
+                    } else {
+                        tma_load_2d(sa, &tmA, fb, ks * BK, ti.row0);
+                    }
+                    tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk0 + ks));
+                    tma_load_3d(sb + B_HALF, &tmB, fb, 0, 0, (int)(blk1 + ks));
+                    bulk_copy_g2s(smem + OFF_SFA + stage * SFA_STAGE, a_sf + (ks >> 2) * SFA_STAGE, SFA_STAGE, fb);
+                    uint8_t *sfb = smem + OFF_SFB + stage * SFB_STAGE;
+                    bulk_copy_g2s(sfb, g.b_scale + (blk0 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
+                    bulk_copy_g2s(sfb + 512, g.b_scale + (blk1 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         uint32_t stage = 0, phase = 0, acc_phase = 0;
@@ -220,7 +244,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    fence_proxy_async_smem();
                     const uint32_t sfa = sbase + OFF_SFA + stage * SFA_STAGE;
                     const uint32_t sfb = sbase + OFF_SFB + stage * SFB_STAGE;
                     tc_cp_32x128b_warpx4(tmem + SFA_COL, sdesc_sf(sfa));
@@ -254,10 +277,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;                    // tensor-memory lane quarter of this warp
+        // Eight warps: warp w reads tensor-memory lanes 32 * (w % 4) ..; the two
+        // warps of a lane quarter split the columns (half = 0 or 1).  Each
+        // thread copies its accumulator slice to registers, releases the
+        // accumulator (so the next tile's MMAs start), then finishes.
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int r = q * 32 + lane;               // accumulator row = pair row in the tile
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL;
-        uint32_t acc_phase = 0;
+        uint32_t acc_phase = 0, tpar = 0;
         for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
             const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb);
             if (!mbar_wait(acc_full, acc_phase, tmo, abort_flag)) {
@@ -267,31 +295,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const size_t row = (size_t)ti.row0 + r;
             if (MODE == 1) {
-                float h[128];
-#pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    uint32_t gr[32], ur[32];
-                    tmem_ld32(trow + 32 * c, gr);
-                    tmem_ld32(trow + 128 + 32 * c, ur);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        const float gv = __uint_as_float(gr[i]);
-                        const float uv = __uint_as_float(ur[i]);
-                        h[32 * c + i] = gv / (1.0f + expf(-gv)) * uv;
-                    }
-                }
+                // channels [64 * half, 64 * half + 64) of the tile's 128: gate
+                // columns at 64 * half, up columns at 128 + 64 * half
+                uint32_t g0[32], g1[32], u0[32], u1[32];
+                tmem_ld32(trow + 64 * half, g0);
+                tmem_ld32(trow + 64 * half + 32, g1);
+                tmem_ld32(trow + 128 + 64 * half, u0);
+                tmem_ld32(trow + 128 + 64 * half + 32, u1);
+                tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(acc_empty);
+                // SwiGLU with the hardware exp2 and reciprocal approximations
+                // (a few ulp of fp32); h is rounded to E4M3 (3 mantissa bits)
+                // right below, so this error is about 1e-4 of the FP8 step.
+                // The accurate library exp and IEEE division, unrolled 64
+                // times, made the epilogue code large enough to slow the
+                // producer and MMA warps that share the SM's instruction cache.
+                float h[64];
                 float amax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 128; i++) amax = fmaxf(amax, fabsf(h[i]));
+                for (int i = 0; i < 32; i++) {
+                    const float ga = __uint_as_float(g0[i]), gb = __uint_as_float(g1[i]);
+                    h[i] = __fdividef(ga, 1.0f + __expf(-ga)) * __uint_as_float(u0[i]);
+                    h[32 + i] = __fdividef(gb, 1.0f + __expf(-gb)) * __uint_as_float(u1[i]);
+                    amax = fmaxf(amax, fmaxf(fabsf(h[i]), fabsf(h[32 + i])));
+                }
+                // the 128-channel amax spans both halves: swap partial maxima
+                // through shared memory (slots alternate between tiles) and a
+                // per-quarter barrier whose phase i belongs to this CTA's tile i
+                float *xa = s_amax + tpar * 2 * BM;
+                xa[half * BM + r] = amax;
+                mbar_arrive(&xbar[q]);
+                if (!mbar_wait(&xbar[q], tpar, tmo, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                amax = fmaxf(amax, xa[(1 - half) * BM + r]);
                 const int e = e4m3_scale_exp(amax);
                 const float s = exp2i(-e);
                 if (r < ti.valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(g.hq + row * out_dim + (size_t)ti.n_block * 128);
+                    uint4 *dst =
+                        reinterpret_cast<uint4 *>(g.hq + row * out_dim + (size_t)ti.n_block * 128 + 64 * half);
 #pragma unroll
-                    for (int v = 0; v < 8; v++) {
+                    for (int v = 0; v < 4; v++) {
                         uint32_t w[4];
 #pragma unroll
                         for (int u = 0; u < 4; u++) {
@@ -300,28 +346,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    g.hs[row * g.hs_stride + ti.n_block] = (uint8_t)(e + 127);
+                    if (half == 0)
+                        g.hs_tiles[((size_t)ti.m_tile * stage_groups(out_dim) + (ti.n_block >> 2)) * SFA_STAGE +
+                                   sf_byte(r, ti.n_block & 3)] = (uint8_t)(e + 127);
                 }
             } else {
-                uint32_t pk[128];
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    uint32_t v[32];
-                    tmem_ld32(trow + 32 * c, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        pk[16 * c + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                }
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(trow + 128 * half, v0);
+                tmem_ld32(trow + 128 * half + 32, v1);
+                tmem_ld32(trow + 128 * half + 64, v2);
+                tmem_ld32(trow + 128 * half + 96, v3);
+                tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(acc_empty);
                 if (r < ti.valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(g.y + row * out_dim + (size_t)ti.n_block * BN);
+                    uint4 *dst = reinterpret_cast<uint4 *>(g.y + row * out_dim + (size_t)ti.n_block * BN + 128 * half);
 #pragma unroll
-                    for (int v = 0; v < 32; v++) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int c = 0; c < 4; c++) {
+                        const uint32_t *v = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            const int b = 8 * j;
+                            dst[4 * c + j] = make_uint4(pack_bf16x2(__uint_as_float(v[b]), __uint_as_float(v[b + 1])),
+                                                        pack_bf16x2(__uint_as_float(v[b + 2]), __uint_as_float(v[b + 3])),
+                                                        pack_bf16x2(__uint_as_float(v[b + 4]), __uint_as_float(v[b + 5])),
+                                                        pack_bf16x2(__uint_as_float(v[b + 6]), __uint_as_float(v[b + 7])));
+                        }
+                    }
                 }
             }
             acc_phase ^= 1u;
+            tpar ^= 1u;
         }
     }
 
@@ -355,30 +410,31 @@ static EncodeTiledFn get_encode_fn()
     return fn;
 }
 
-// A operand: E4M3 rows [rows][K], 128 x 128 box, 128-byte swizzle.
-static bool make_map_a(CUtensorMap *m, const uint8_t *a, long long rows, int K)
+// A operand: E4M3 rows [rows][K], 128-channel x box_rows box, 128-byte swizzle.
+static bool make_map_a(CUtensorMap *m, const uint8_t *a, long long rows, int K, int box_rows)
 {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K};
-    cuuint32_t box[2] = {(cuuint32_t)gg::BK, (cuuint32_t)gg::BM};
+    cuuint32_t box[2] = {(cuuint32_t)gg::BK, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// B operand: packed E2M1 [E][N][K/2]; the copy engine spreads each 8-byte
-// group of 16 codes over 16 bytes of shared memory, the layout the FP8/FP6/FP4
-// MMA reads.  128 x 128 box, 128-byte swizzle.
-static bool make_map_b(CUtensorMap *m, const uint8_t *b, int E, int N, int K)
+// B operand: tiled MXFP4 codes, 128 x 128 blocks of 8 KB (row r at r * 64);
+// the copy engine spreads each 8-byte group of 16 codes over 16 bytes of
+// shared memory, the layout the FP8/FP6/FP4 MMA reads.  One block per box,
+// 128-byte swizzle.
+static bool make_map_b(CUtensorMap *m, const uint8_t *b, long long blocks)
 {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)E};
-    cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)N * (cuuint64_t)K / 2};
-    cuuint32_t box[3] = {(cuuint32_t)gg::BK, 128, 1};
+    cuuint64_t dims[3] = {128, 128, (cuuint64_t)blocks};
+    cuuint64_t strides[2] = {64, (cuuint64_t)kBlockCodeBytes};
+    cuuint32_t box[3] = {128, 128, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t *>(b), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -389,9 +445,10 @@ template <int MODE>
 static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
 {
     if (a.P == 0) return cudaSuccess;
-    CUtensorMap ma, mb;
-    if (!make_map_a(&ma, a.a, a.P, a.K)) return cudaErrorInvalidValue;
-    if (!make_map_b(&mb, a.b, a.E, a.N, a.K)) return cudaErrorInvalidValue;
+    CUtensorMap ma, ma16, mb;
+    if (!make_map_a(&ma, a.a, a.P, a.K, gg::BM)) return cudaErrorInvalidValue;
+    if (!make_map_a(&ma16, a.a, a.P, a.K, gg::A_SMALL_ROWS)) return cudaErrorInvalidValue;
+    if (!make_map_b(&mb, a.b, (long long)a.E * (a.N / 128) * (a.K / 128))) return cudaErrorInvalidValue;
     auto kern = gg::grouped_gemm_kernel<MODE>;
     static bool attr_set[2] = {false, false};
     if (!attr_set[MODE - 1]) {
@@ -402,7 +459,7 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     const int nb = (MODE == 1) ? out_dim / 128 : out_dim / gg::BN;
     const long long tiles = max_row_tiles(a.P, a.E) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
-    kern<<<grid, gg::NUM_THREADS, gg::SMEM_BYTES, st>>>(ma, mb, a, out_dim);
+    kern<<<grid, gg::NUM_THREADS, gg::SMEM_BYTES, st>>>(ma, ma16, mb, a, out_dim);
     return cudaGetLastError();
 }
 

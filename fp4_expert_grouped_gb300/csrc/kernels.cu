@@ -18,12 +18,15 @@
 namespace fp4moe {
 
 // ---------------------------------------------------------------------------
-// MXFP4 packing.  One thread per 8 consecutive K elements; four threads share
-// a 32-element block (scale X = floor(log2 amax) - 2, codes = RNE E2M1 of
-// w * 2^-X saturated to +-6, low nibble = even element).
+// MXFP4 packing into the tiled layout (moe_internal.h).  One thread per 8
+// consecutive K elements; four threads share a 32-element block (scale
+// X = floor(log2 amax) - 2, codes = RNE E2M1 of w * 2^-X saturated to +-6,
+// low nibble = even element).  The codes of row n, columns k..k+7 land at
+// block b = (e * N/128 + n/128) * K/128 + k/128, row n % 128, byte (k % 128)/2;
+// the scale byte at b * 512 + sf_byte(n % 128, (k % 128) / 32).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pack_fp4_kernel(const float *__restrict__ w, uint8_t *__restrict__ w_fp4,
-                                                       uint8_t *__restrict__ w_scale, long long n8)
+                                                       uint8_t *__restrict__ w_scale, long long n8, int N, int K)
 {
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = gid < n8;
@@ -50,18 +53,24 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(const float *__restrict__
 #pragma unroll
     for (int i = 0; i < 4; i++) codes |= cvt_e2m1x2(v[2 * i] * s, v[2 * i + 1] * s) << (8 * i);
     if (valid) {
-        reinterpret_cast<uint32_t *>(w_fp4)[gid] = codes;
-        if ((gid & 3) == 0) w_scale[gid >> 2] = (uint8_t)(X + 127);
+        const long long el = gid * 8;
+        const long long row = el / K;                  // e * N + n
+        const int k0 = (int)(el % K);
+        const long long e = row / N;
+        const int n = (int)(row % N);
+        const long long blk = (e * (N / 128) + n / 128) * (K / 128) + k0 / 128;
+        const int r = n % 128;
+        *reinterpret_cast<uint32_t *>(w_fp4 + blk * kBlockCodeBytes + r * 64 + (k0 % 128) / 2) = codes;
+        if ((gid & 3) == 0) w_scale[blk * kBlockScaleBytes + sf_byte(r, (k0 % 128) / 32)] = (uint8_t)(X + 127);
     }
 }
 
-cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, long long rows, int K,
-                            cudaStream_t st)
+cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E, int N, int K, cudaStream_t st)
 {
-    const long long n8 = rows * (long long)(K / 8);
+    const long long n8 = (long long)E * N * (K / 8);
     if (n8 == 0) return cudaSuccess;
     const long long blocks = (n8 + 255) / 256;
-    pack_fp4_kernel<<<(unsigned)blocks, 256, 0, st>>>(w, w_fp4, w_scale, n8);
+    pack_fp4_kernel<<<(unsigned)blocks, 256, 0, st>>>(w, w_fp4, w_scale, n8, N, K);
     return cudaGetLastError();
 }
 
@@ -494,31 +503,44 @@ cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_
 
 // ---------------------------------------------------------------------------
 // Dispatch copy: row `pos` of the expert-ordered activations is the quantised
-// row of token sorted_pair[pos] / k (one warp per row, 16-byte vectors).
+// row of token sorted_pair[pos] / k (one warp per row, 16-byte vectors).  Its
+// scales go to the per-tile layout the GEMM's scale copy reads: tile
+// m = tile_prefix[e] + local / 128, row r = local % 128, group g of four
+// 128-channel stages -> 4 bytes at (m * G + g) * 512 + sf_byte(r, 0).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) dispatch_kernel(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xs,
                                                        int xs_stride, const int32_t *__restrict__ sorted_pair,
-                                                       uint8_t *__restrict__ xq_sorted, uint8_t *__restrict__ xs_sorted,
+                                                       const int32_t *__restrict__ topk_idx,
+                                                       const int32_t *__restrict__ expert_offsets,
+                                                       const int32_t *__restrict__ tile_prefix,
+                                                       uint8_t *__restrict__ xq_sorted, uint8_t *__restrict__ xs_tiles,
                                                        long long P, int d, int k)
 {
     const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (pos >= P) return;
     const int lane = threadIdx.x & 31;
-    const int t = __ldg(sorted_pair + pos) / k;
+    const int p = __ldg(sorted_pair + pos);
+    const int t = p / k;
     const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)t * d);
     uint4 *dst = reinterpret_cast<uint4 *>(xq_sorted + (size_t)pos * d);
     for (int i = lane; i < d / 16; i += 32) dst[i] = __ldg(src + i);
+    const int e = __ldg(topk_idx + p);
+    const long long local = pos - __ldg(expert_offsets + e);
+    const long long m = __ldg(tile_prefix + e) + local / kTileM;
+    const int r = (int)(local % kTileM);
+    const int G = stage_groups(d);
     const uint32_t *ss = reinterpret_cast<const uint32_t *>(xs + (size_t)t * xs_stride);
-    uint32_t *sd = reinterpret_cast<uint32_t *>(xs_sorted + (size_t)pos * xs_stride);
-    for (int i = lane; i < xs_stride / 4; i += 32) sd[i] = __ldg(ss + i);
+    for (int g = lane; g < G; g += 32)
+        *reinterpret_cast<uint32_t *>(xs_tiles + ((size_t)m * G + g) * kBlockScaleBytes + sf_byte(r, 0)) = __ldg(ss + g);
 }
 
 cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride, const int32_t *sorted_pair,
-                            uint8_t *xq_sorted, uint8_t *xs_sorted, long long P, int d, int k, cudaStream_t st)
+                            const int32_t *topk_idx, const int32_t *expert_offsets, const int32_t *tile_prefix,
+                            uint8_t *xq_sorted, uint8_t *xs_tiles, long long P, int d, int k, cudaStream_t st)
 {
     if (P == 0) return cudaSuccess;
-    dispatch_kernel<<<(unsigned)((P + 7) / 8), 256, 0, st>>>(xq, xs, xs_stride, sorted_pair, xq_sorted, xs_sorted, P,
-                                                             d, k);
+    dispatch_kernel<<<(unsigned)((P + 7) / 8), 256, 0, st>>>(xq, xs, xs_stride, sorted_pair, topk_idx, expert_offsets,
+                                                             tile_prefix, xq_sorted, xs_tiles, P, d, k);
     return cudaGetLastError();
 }
 

@@ -113,23 +113,13 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// 4-byte asynchronous global -> shared copy (cp.async, completion tracked per thread).
-__device__ __forceinline__ void cp_async_4(void *dst, const void *src)
+// Contiguous global -> shared bulk copy completing on `bar` (16-byte aligned,
+// size a multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-
-// Arrive on `bar` once all of this thread's earlier cp.async copies have landed
-// (the barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Make generic-proxy shared-memory writes visible to the async proxy (tensor core reads).
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 // ---------------------------------------------------------------------------

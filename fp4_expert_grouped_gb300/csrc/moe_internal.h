@@ -20,6 +20,23 @@ constexpr int kTileM = 128;   // pair rows (tokens) per tile = MMA M
 constexpr int kTileN = 256;   // weight rows per tile = MMA N
 constexpr int kTileK = 128;   // K per pipeline stage
 
+// Tiled MXFP4 weight layout written by moe_pack_fp4 (see fp4moe.h): the
+// matrix [N][K] of an expert is cut into 128 x 128 blocks, numbered
+// ((e * N/128 + n/128) * K/128 + k/128).  Block b holds
+//   codes:  8192 bytes at b * 8192, row r (0..127) at r * 64, two codes per
+//           byte, low nibble = even k
+//   scales: 512 bytes at b * 512, the UE8M0 byte of row r and 32-element
+//           sub-block j (0..3) at (r % 32) * 16 + (r / 32) * 4 + j -- the
+//           order the tensor-core scale-factor copy reads.
+constexpr int kBlockCodeBytes = 128 * 64;
+constexpr int kBlockScaleBytes = 512;
+__host__ __device__ inline int sf_byte(int r, int j) { return (r % 32) * 16 + (r / 32) * 4 + j; }
+
+// Activation scales of the GEMM operands (xq rows for GEMM1, hq rows for
+// GEMM2) use the same 512-byte order per 128-row tile and per group of four
+// 128-channel stages: byte j of row r in group g is the scale of stage 4g + j.
+__host__ __device__ inline int stage_groups(int K) { return (K / 128 + 3) / 4; }
+
 struct Shapes {
     int T, d, inter, E, k;
     long long P() const { return (long long)T * k; }
@@ -33,13 +50,19 @@ struct Workspace {
 };
 bool workspace_layout(const Shapes &s, Workspace *ws);
 
-// Row strides of the per-row scale arrays used by the GEMM (multiple of 4 so a
-// 4-byte word covers four consecutive 128-channel groups).
+// Row stride of the per-token scale array written by the top-k kernel
+// (a multiple of 4 so one 32-bit word holds four consecutive groups).
 inline int scale_row_stride(int channels) { return ((channels / 128) + 3) / 4 * 4; }
 
+// upper bound on the number of 128-row tiles of the expert-ordered pairs
+inline long long max_row_tiles(long long P, int E)
+{
+    return (P + kTileM - 1) / kTileM + (P < E ? P : E);
+}
+
 // ---- launchers (kernels.cu) ----------------------------------------------
-cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, long long rows, int K,
-                            cudaStream_t st);
+// rows = E * N; writes the tiled layout above (N % 128 == 0, K % 128 == 0)
+cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E, int N, int K, cudaStream_t st);
 cudaError_t launch_quantize(const uint16_t *x, uint8_t *xq, uint8_t *xs, int xs_stride, int T, int d,
                             cudaStream_t st);
 cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T, int d,
@@ -51,19 +74,21 @@ cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const 
 // dispatch plan; tile_prefix may be NULL.
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
                         int32_t *tile_prefix, int T, int E, int k, unsigned *status, cudaStream_t st);
-// copy every pair's quantised token row into expert order
+// copy every pair's quantised token row into expert order and its scales into
+// the per-tile scale layout
 cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride, const int32_t *sorted_pair,
-                            uint8_t *xq_sorted, uint8_t *xs_sorted, long long P, int d, int k, cudaStream_t st);
+                            const int32_t *topk_idx, const int32_t *expert_offsets, const int32_t *tile_prefix,
+                            uint8_t *xq_sorted, uint8_t *xs_tiles, long long P, int d, int k, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,
                            int d, int k, cudaStream_t st);
 
 // ---- grouped GEMMs (gemm.cu) ---------------------------------------------
 struct GemmArgs {
-    // A: pair rows in expert order, E4M3 [P][K] with per-row scales [P][a_scale_stride]
+    // A: pair rows in expert order, E4M3 [P][K]; scales per 128-row tile in
+    // the 512-byte order, [tiles][stage_groups(K)][512]
     const uint8_t *a;
-    const uint8_t *a_scale;
-    int a_scale_stride;
-    // B: packed weights of all experts [E][N][K/2] + UE8M0 scales [E][N][K/32]
+    const uint8_t *a_scale_tiles;
+    // B: tiled MXFP4 weights of all experts (codes + scales), N rows, K columns
     const uint8_t *b;
     const uint8_t *b_scale;
     int N;
@@ -73,10 +98,10 @@ struct GemmArgs {
     const int32_t *tile_prefix;      // [E+1]
     int E;
     long long P;
-    // outputs: GEMM1 -> hq [P][inter] + hs [P][hs_stride]; GEMM2 -> y bf16 [P][d]
+    // outputs: GEMM1 -> hq [P][inter] + hs tiles [tiles][stage_groups(inter)][512];
+    // GEMM2 -> y bf16 [P][d]
     uint8_t *hq;
-    uint8_t *hs;
-    int hs_stride;
+    uint8_t *hs_tiles;
     uint16_t *y;
     unsigned *status;
     unsigned long long timeout_ns;
@@ -84,10 +109,5 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st);
 cudaError_t launch_gemm2(const GemmArgs &a, int d, cudaStream_t st);
-// upper bound on the number of tiles for the persistent grid size
-inline long long max_row_tiles(long long P, int E)
-{
-    return (P + kTileM - 1) / kTileM + (P < E ? P : E);
-}
 
 } // namespace fp4moe

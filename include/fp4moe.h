@@ -67,17 +67,25 @@ const char *moe_status_string(moe_status s);
 int moe_version(void);
 
 /*
- * moe_pack_fp4 -- MXFP4 weight quantisation (first page, section 4).
+ * moe_pack_fp4 -- MXFP4 weight quantisation (first page, section 4) into the
+ * tiled layout moe_forward reads.
  *   w        device, fp32 [E][N][K] row-major (K contiguous)
- *   w_fp4    device, uint8 [E][N][K/2]: two E2M1 codes per byte, the low
- *            nibble holds the even K index
- *   w_scale  device, uint8 [E][N][K/32]: UE8M0 byte X + 127 per 32 K-elements,
- *            X = floor(log2(max |w| of the block)) - 2 (X = -127 for an all-zero
- *            block), clamped to [-127, 127]; codes are the round-to-nearest-even
- *            E2M1 of w * 2^-X saturated to +-6.
+ *   rule     per 32 consecutive K-elements: X = floor(log2(max |w|)) - 2
+ *            (X = -127 for an all-zero block), clamped to [-127, 127]; codes
+ *            are the round-to-nearest-even E2M1 of w * 2^-X saturated to +-6,
+ *            the scale is the UE8M0 byte X + 127.
+ *   layout   each expert's [N][K] matrix is cut into 128 x 128 blocks,
+ *            numbered b = (e * N/128 + n/128) * K/128 + k/128:
+ *   w_fp4    device, E*N*K/2 bytes: block b at b * 8192, its row n % 128 at
+ *            (n % 128) * 64, two codes per byte, the low nibble holding the
+ *            even k (so one block is 8 KB of contiguous memory)
+ *   w_scale  device, E*N*K/32 bytes: block b at b * 512, the scale of row
+ *            r = n % 128 and 32-element sub-block j = (k % 128) / 32 at byte
+ *            (r % 32) * 16 + (r / 32) * 4 + j (the order the tensor cores'
+ *            scale-factor copy reads, so the forward loads it with one copy)
  * For the layer: W13 is [E][2*inter][d] (rows 0..inter-1 = gate projection,
  * inter..2*inter-1 = up projection), W2 is [E][d][inter].
- * Requires K % 32 == 0, E, N >= 1.  Load-time operation, off the hot path.
+ * Requires N % 128 == 0, K % 128 == 0.  Load-time operation, off the hot path.
  */
 moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale,
                         int E, int N, int K, void *stream);
@@ -157,8 +165,8 @@ moe_status moe_dispatch_plan(const int32_t *topk_idx, int32_t *expert_offsets,
  * over slots j = 0..k-1 of w_j * y_j).
  *   x                  device, bf16 [T][d]
  *   gate_w             device, fp32 [d][E]
- *   w13_fp4, w13_scale device, moe_pack_fp4 output for W13 [E][2*inter][d]
- *   w2_fp4,  w2_scale  device, moe_pack_fp4 output for W2 [E][d][inter]
+ *   w13_fp4, w13_scale device, moe_pack_fp4 output (tiled) for W13 [E][2*inter][d]
+ *   w2_fp4,  w2_scale  device, moe_pack_fp4 output (tiled) for W2 [E][d][inter]
  *   out                device, bf16 [T][d]
  * Workspace (moe_workspace_size bytes) is allocated stream-ordered on `stream`
  * and released on it before return.
@@ -223,10 +231,13 @@ enum {
     MOE_WS_PAIR_POS,      /* int32 [P] */
     MOE_WS_TILE_PREFIX,   /* int32 [E+1] running count of 128-row tiles */
     MOE_WS_HQ,            /* uint8 E4M3 [P][inter], rows in expert order */
-    MOE_WS_HS,            /* uint8 [P][stride], first inter/128 bytes used */
+    MOE_WS_HS_TILES,      /* uint8 scales of hq per 128-row tile m and group g
+                             of four 128-channel groups: 512-byte blocks at
+                             (m * ceil(inter/512) + g) * 512, the byte of row r
+                             and group 4g + j at (r % 32) * 16 + (r / 32) * 4 + j */
     MOE_WS_Y,             /* bf16 [P][d], rows in expert order */
     MOE_WS_XQ_SORTED,     /* uint8 E4M3 [P][d]: row p = xq of the pair's token, expert order */
-    MOE_WS_XS_SORTED,     /* uint8 [P][stride], scales of those rows */
+    MOE_WS_XS_TILES,      /* scales of those rows, laid out like MOE_WS_HS_TILES with d */
     MOE_WS_COUNT
 };
 size_t moe_workspace_layout(int T, int d, int inter, int E, int k,

@@ -25,3 +25,27 @@ def read_golden(name):
                 continue
             rows.append(line.split())
     return rows
+
+
+# ---- the tiled MXFP4 byte order of moe_pack_fp4 (include/fp4moe.h) ---------
+# A pure permutation of the plain layout the oracle writes ([E][N][K/2] codes,
+# [E][N][K/32] scales), used to compare the two bit for bit.
+
+def tile_codes(fp4):
+    """plain codes [E][N][K/2] -> tiled bytes [E][N/128][K/128][128 rows][64]."""
+    import numpy as np
+    E, N, K2 = fp4.shape
+    return np.ascontiguousarray(fp4.reshape(E, N // 128, 128, K2 // 64, 64).transpose(0, 1, 3, 2, 4))
+
+
+def tile_scales(sc):
+    """plain scales [E][N][K/32] -> tiled bytes [E][N/128][K/128][512], the byte of
+    row r and sub-block j at (r % 32) * 16 + (r / 32) * 4 + j."""
+    import numpy as np
+    E, N, K32 = sc.shape
+    a = sc.reshape(E, N // 128, 4, 32, K32 // 4, 4)          # (e, nb, r/32, r%32, kt, j)
+    return np.ascontiguousarray(a.transpose(0, 1, 4, 3, 2, 5)).reshape(E, N // 128, K32 // 4, 512)
+
+
+def sf_byte(r, j):
+    return (r % 32) * 16 + (r // 32) * 4 + j

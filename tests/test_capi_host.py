@@ -84,9 +84,10 @@ def test_forward_argument_checks(capi):
 
 def test_other_entry_points_reject_bad_arguments(capi):
     lib = capi.lib()
-    assert lib.moe_pack_fp4(None, FAKE, FAKE, 1, 1, 32, None) == 1
-    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 1, 48, None) == 2
-    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 0, 1, 32, None) == 0
+    assert lib.moe_pack_fp4(None, FAKE, FAKE, 1, 128, 128, None) == 1
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 128, 96, None) == 2     # K % 128
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 64, 128, None) == 2     # N % 128
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 0, 128, 128, None) == 0
     assert lib.moe_quantize_act(FAKE, FAKE, FAKE, 4, 100, None) == 2
     assert lib.moe_quantize_act(FAKE, FAKE, FAKE, 0, 128, None) == 0
     assert lib.moe_route(FAKE, FAKE, None, FAKE, FAKE, 4, 128, 8, 9, None) == 2
@@ -102,14 +103,15 @@ def test_workspace_layout(capi):
         assert total == capi.moe_workspace_size(T, d, inter, E, k) > 0
         P = T * k
         xs = ((d // 128) + 3) // 4 * 4
-        hs = ((inter // 128) + 3) // 4 * 4
+        tiles = (P + 127) // 128 + min(P, E)
+        gx, gh = (d // 128 + 3) // 4, (inter // 128 + 3) // 4
         sizes = [T * d, T * xs, T * E * 4, P * 4, P * 4, (E + 1) * 4, P * 4, P * 4, (E + 1) * 4,
-                 P * inter, P * hs, P * d * 2, P * d, P * xs]
+                 P * inter, tiles * gh * 512, P * d * 2, P * d, tiles * gx * 512]
         assert len(sizes) == capi.MOE_WS_COUNT
         for i in range(capi.MOE_WS_COUNT):
             assert off[i] % 256 == 0
             end = off[i] + sizes[i]
             nxt = off[i + 1] if i + 1 < capi.MOE_WS_COUNT else total
             assert end <= nxt
-        assert st[capi.MOE_WS_XS] == xs and st[capi.MOE_WS_HS] == hs and st[capi.MOE_WS_Y] == 2 * d
+        assert st[capi.MOE_WS_XS] == xs and st[capi.MOE_WS_HS_TILES] == gh * 512 and st[capi.MOE_WS_Y] == 2 * d
     assert capi.moe_workspace_size(8, 384, 128, 8, 2) == 0

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import oracle
+from conftest import sf_byte, tile_codes, tile_scales
 from fp4_expert_grouped_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -51,6 +52,13 @@ def check_layer_tolerance(got_bits, ref_bits, what=""):
     assert rel.max() <= 5e-3, "%s worst token rel L2 %g" % (what, rel.max())
 
 
+def assert_packs_equal(g_fp4, g_scale, o_fp4, o_scale):
+    """GPU packs (tiled byte order) equal the oracle's plain packs after the
+    tiling permutation."""
+    assert np.array_equal(g_fp4.cpu().numpy().reshape(-1), tile_codes(o_fp4).reshape(-1))
+    assert np.array_equal(g_scale.cpu().numpy().reshape(-1), tile_scales(o_scale).reshape(-1))
+
+
 def small_case(T, d, inter, E, k, seed, bias=False):
     w = inputs.Workload("case", T, d, inter, E, k, seed, zipf_bias=bias)
     x, gw, b = inputs.make_x_gate(w, "cpu")
@@ -66,8 +74,8 @@ def run_small_forward(w, x, gw, b, w13, w2):
     xb = inputs.bf16_bits(x)
     f13, s13 = oracle.pack_fp4(w13.numpy())
     f2, s2 = oracle.pack_fp4(w2.numpy())
-    assert np.array_equal(pk.w13_fp4.cpu().numpy(), f13) and np.array_equal(pk.w13_scale.cpu().numpy(), s13)
-    assert np.array_equal(pk.w2_fp4.cpu().numpy(), f2) and np.array_equal(pk.w2_scale.cpu().numpy(), s2)
+    assert_packs_equal(pk.w13_fp4, pk.w13_scale, f13, s13)
+    assert_packs_equal(pk.w2_fp4, pk.w2_scale, f2, s2)
     ref, ridx, rw = oracle.moe_forward(xb, gw.numpy(), f13, s13, f2, s2, w.k, None if b is None else b.numpy())
     assert np.array_equal(ti.cpu().numpy(), ridx)
     assert np.allclose(tw.cpu().numpy(), rw, rtol=2e-7, atol=0)
@@ -83,7 +91,7 @@ def run_small_forward(w, x, gw, b, w13, w2):
 
 def test_pack_fp4_bitexact_special_values():
     rng = np.random.default_rng(100)
-    E, N, K = 3, 40, 512
+    E, N, K = 3, 256, 512
     w = rng.normal(0, 0.03, (E, N, K)).astype(np.float32)
     w[0, 0, :32] = 0.0
     w[0, 1, :32] = -0.0
@@ -99,13 +107,13 @@ def test_pack_fp4_bitexact_special_values():
     w[2, 7, 7] = 6.0
     w[2, 8, :7] = -mids
     w[2, 8, 7] = 6.0
+    w[2, 200, 300:332] = np.float32(3.0)                  # a row and column in the second block
     wt = torch.from_numpy(w).to(DEV)
     fp4 = torch.empty((E, N, K // 2), dtype=torch.uint8, device=DEV)
     sc = torch.empty((E, N, K // 32), dtype=torch.uint8, device=DEV)
     capi().moe_pack_fp4(wt, fp4, sc)
     of, os_ = oracle.pack_fp4(w)
-    assert np.array_equal(sc.cpu().numpy(), os_)
-    assert np.array_equal(fp4.cpu().numpy(), of)
+    assert_packs_equal(fp4, sc, of, os_)
 
 
 def test_quantize_act_bitexact():
@@ -237,10 +245,8 @@ def _sampled_oracle(w, x, gw, bias, tokens, pk_gpu):
         a, b = inputs.make_expert(w, e, DEV)
         f13[e], s13[e] = [v[0] for v in oracle.pack_fp4(a.cpu().numpy()[None])]
         f2[e], s2[e] = [v[0] for v in oracle.pack_fp4(b.cpu().numpy()[None])]
-        assert np.array_equal(pk_gpu.w13_fp4[e].cpu().numpy(), f13[e])
-        assert np.array_equal(pk_gpu.w13_scale[e].cpu().numpy(), s13[e])
-        assert np.array_equal(pk_gpu.w2_fp4[e].cpu().numpy(), f2[e])
-        assert np.array_equal(pk_gpu.w2_scale[e].cpu().numpy(), s2[e])
+        assert_packs_equal(pk_gpu.w13_fp4[e], pk_gpu.w13_scale[e], f13[e:e + 1], s13[e:e + 1])
+        assert_packs_equal(pk_gpu.w2_fp4[e], pk_gpu.w2_scale[e], f2[e:e + 1], s2[e:e + 1])
     ref, idx, wts = oracle.moe_forward(xb, gwn, f13, s13, f2, s2, w.k, bn, tokens=np.asarray(tokens, np.int32))
     return ref, idx, wts
 
@@ -332,10 +338,17 @@ def test_workspace_intermediates_tiny():
     f13, s13 = oracle.pack_fp4(w13.numpy())
     f2, s2 = oracle.pack_fp4(w2.numpy())
     hq = wsn[off[c.MOE_WS_HQ]:][:w.P * w.inter].reshape(w.P, w.inter)
-    hs = wsn[off[c.MOE_WS_HS]:][:w.P * st[c.MOE_WS_HS]].reshape(w.P, -1)[:, :w.inter // 128]
-    deq = torch.from_numpy(hq.copy()).view(torch.float8_e4m3fn).double().numpy().reshape(w.P, -1, 128)
-    deq = (deq * np.exp2(hs.astype(np.float64) - 127)[..., None]).reshape(w.P, -1)
+    tp = wsn[off[c.MOE_WS_TILE_PREFIX]:][:4 * (w.E + 1)].view(np.int32)
+    assert np.array_equal(tp, np.concatenate([[0], np.cumsum((np.diff(offs) + 127) // 128)]))
+    hs_tiles = wsn[off[c.MOE_WS_HS_TILES]:]
+    GH = (w.inter // 128 + 3) // 4
     for pos in range(w.P):
         t, j = divmod(int(sp[pos]), w.k)
+        e = ridx[t, j]
+        local = pos - offs[e]
+        m, r = tp[e] + local // 128, local % 128
+        hs = np.array([hs_tiles[(m * GH + nb // 4) * 512 + sf_byte(r, nb % 4)] for nb in range(w.inter // 128)])
+        deq = torch.from_numpy(hq[pos].copy()).view(torch.float8_e4m3fn).double().numpy().reshape(-1, 128)
+        deq = (deq * np.exp2(hs.astype(np.float64) - 127)[:, None]).reshape(-1)
         h, _, _, _ = oracle.expert_pair(oq[t], os_[t], ridx[t, j], f13, s13, f2, s2)
-        assert np.linalg.norm(deq[pos] - h) <= 0.05 * np.linalg.norm(h) + 1e-30
+        assert np.linalg.norm(deq - h) <= 0.05 * np.linalg.norm(h) + 1e-30
