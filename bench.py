@@ -8,10 +8,14 @@ FP8 re-quantisation), grouped GEMM2 and the combine -- every stage of the layer.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
   python bench.py --impl reference ...     # the CPU oracle on the host cores
 
-Timing: W untimed warm-up steps, then K steps, each timed with CUDA events on
-the launching stream (the library records one event between every two stages),
-with a 256 MiB write between steps to flush L2; barrier + synchronize on both
-sides of the timed loop; the per-step time is the max over ranks.  Under
+Timing: W untimed warm-up steps, then K steps, each timed with a pair of CUDA
+events on the launching stream, with a 256 MiB write between steps to flush
+L2; barrier + synchronize on both sides of the timed loop; the per-step time
+is the max over ranks.  A second pass of K steps records an event between
+every two stages (the library does it when given events) for the per-stage
+times and the dominant kernel's roofline fraction; those events stop the
+stages from overlapping their launches, so that pass is slightly slower and is
+reported separately.  Under
 torchrun (N > 1) every rank runs its own replica of the workload (token-sharded
 data parallelism: there is no exchange between ranks), so scaling is weak.
 """
@@ -306,7 +310,12 @@ def run_ours(args, w, world, rank, local):
     if st != 0:
         raise RuntimeError("device status after warm-up: " + capi.moe_status_string(st))
 
-    events = [new_events() for _ in range(args.steps)]
+    # Timed region 1 (the headline number): one event pair per step around the
+    # whole forward.  No events between the stages here: an event record
+    # between two kernels stops the next one from launching early
+    # (programmatic dependent launch), which costs ~25 us at decode.
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(local)
     dist_barrier()
@@ -314,20 +323,35 @@ def run_ours(args, w, world, rank, local):
     clocks.start()
     for s in range(args.steps):
         flush.zero_()
-        step(events[s])
+        pairs[s][0].record(stream)
+        step(None)
+        pairs[s][1].record(stream)
     torch.cuda.synchronize(dev)
     dist_barrier()
     ck = clocks.stop()
-    st = capi.moe_get_device_status()
-    if st != 0:
-        raise RuntimeError("device status after timed steps: " + capi.moe_status_string(st))
-
-    step_ms = [events[s][0].elapsed_time(events[s][nst]) for s in range(args.steps)]
-    stage_ms = {name: statistics.mean(events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps))
-                for i, name in enumerate(capi.STAGES)}
+    step_ms = [a.elapsed_time(b) for a, b in pairs]
     ms_local = statistics.mean(step_ms)
     ms = dist_max(ms_local, dev)
     value = world * w.T / (ms / 1e3)
+
+    # Timed region 2 (the breakdown): the same steps with an event between
+    # every two stages; gives each kernel's duration, the dominant kernel's
+    # roofline numbers, and the step time with stage events.
+    events = [new_events() for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    dist_barrier()
+    torch.cuda.synchronize(dev)
+    for s in range(args.steps):
+        flush.zero_()
+        step(events[s])
+    torch.cuda.synchronize(dev)
+    dist_barrier()
+    st = capi.moe_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status after timed steps: " + capi.moe_status_string(st))
+    staged_ms = statistics.mean(events[s][0].elapsed_time(events[s][nst]) for s in range(args.steps))
+    stage_ms = {name: statistics.mean(events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps))
+                for i, name in enumerate(capi.STAGES)}
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     x_host = x.cpu().pin_memory()
@@ -385,6 +409,7 @@ def run_ours(args, w, world, rank, local):
                   "TFLOPs": lflops / (ms / 1e3) / 1e12, "touched_experts": touched,
                   "max_expert_load": int(counts.max()), "mean_expert_load": float(counts.mean())},
         "stages_us": {k: v * 1e3 for k, v in stage_ms.items()},
+        "ms_per_step_with_stage_events": staged_ms,
         "e2e": {"value": e2e_v, "unit": UNIT, "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size())},
         "gpu_launches": len(capi.STAGES) * args.steps,

@@ -117,6 +117,8 @@ bool workspace_layout(const Shapes &s, Workspace *ws)
     bytes[MOE_WS_Y] = P * d * 2;             stride[MOE_WS_Y] = d * 2;
     bytes[MOE_WS_XQ_SORTED] = P * d;         stride[MOE_WS_XQ_SORTED] = d;
     bytes[MOE_WS_XS_TILES] = xs_tiles;       stride[MOE_WS_XS_TILES] = stage_groups(s.d) * kBlockScaleBytes;
+    bytes[MOE_WS_PLAN_COUNTS] = plan_scratch_bytes((long long)P, s.E);
+    stride[MOE_WS_PLAN_COUNTS] = (size_t)s.E * 4;
     size_t off = 0;
     for (int i = 0; i < MOE_WS_COUNT; i++) {
         ws->off[i] = off;
@@ -210,8 +212,14 @@ moe_status moe_dispatch_plan(const int32_t *topk_idx, int32_t *expert_offsets, i
     DeviceInfo *di;
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
-    return cuda_status(launch_plan(topk_idx, expert_offsets, sorted_pair, pair_pos, nullptr, T, E, k, di->status,
-                                   (cudaStream_t)stream));
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t scratch = plan_scratch_bytes((long long)T * k, E);
+    void *counts = nullptr;
+    if (scratch && cudaMallocAsync(&counts, scratch, s) != cudaSuccess) return MOE_ERR_WORKSPACE;
+    cudaError_t e = launch_plan(topk_idx, expert_offsets, sorted_pair, pair_pos, nullptr, (int *)counts, T, E, k,
+                                di->status, s);
+    cudaError_t f = counts ? cudaFreeAsync(counts, s) : cudaSuccess;
+    return cuda_status(e != cudaSuccess ? e : f);
 }
 
 size_t moe_workspace_layout(int T, int d, int inter, int E, int k, size_t *offsets, size_t *strides)
@@ -291,7 +299,8 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
         e = launch_topk(logits, topk_idx, topk_w, x, xq, xs, xs_stride, T, d, E, k, di->status, s);
     mark(MOE_STAGE_PLAN);
     if (e == cudaSuccess)
-        e = launch_plan(topk_idx, offs, sorted_pair, pair_pos, tile_prefix, T, E, k, di->status, s);
+        e = launch_plan(topk_idx, offs, sorted_pair, pair_pos, tile_prefix,
+                        reinterpret_cast<int *>(at(MOE_WS_PLAN_COUNTS)), T, E, k, di->status, s);
     mark(MOE_STAGE_DISPATCH);
     if (e == cudaSuccess)
         e = launch_dispatch(xq, xs, xs_stride, sorted_pair, topk_idx, offs, tile_prefix, xq_sorted, xs_tiles, P, d,

@@ -126,10 +126,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
     const int E = g.E;
 
-    for (int i = threadIdx.x; i <= E; i += NUM_THREADS) {
-        s_offs[i] = g.expert_offsets[i];
-        s_tp[i] = g.tile_prefix[i];
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
             mbar_init(&full[s], FULL_ARRIVALS);
@@ -149,6 +145,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) {
         tmem_alloc(tmem_holder, TMEM_COLS);
         tmem_relinquish();
+    }
+    // everything above overlaps the previous kernel's tail; the plan and the
+    // A operand are its outputs
+    pdl_wait();
+    for (int i = threadIdx.x; i <= E; i += NUM_THREADS) {
+        s_offs[i] = g.expert_offsets[i];
+        s_tp[i] = g.tile_prefix[i];
     }
     tc_fence_before();
     __syncthreads();
@@ -380,6 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -459,8 +463,7 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     const int nb = (MODE == 1) ? out_dim / 128 : out_dim / gg::BN;
     const long long tiles = max_row_tiles(a.P, a.E) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
-    kern<<<grid, gg::NUM_THREADS, gg::SMEM_BYTES, st>>>(ma, ma16, mb, a, out_dim);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), gg::SMEM_BYTES, st, ma, ma16, mb, a, out_dim);
 }
 
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm<1>(a, inter, st); }

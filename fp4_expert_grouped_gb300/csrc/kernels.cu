@@ -28,6 +28,7 @@ namespace fp4moe {
 __global__ void __launch_bounds__(256) pack_fp4_kernel(const float *__restrict__ w, uint8_t *__restrict__ w_fp4,
                                                        uint8_t *__restrict__ w_scale, long long n8, int N, int K)
 {
+    pdl_wait();
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = gid < n8;
     float v[8];
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(const float *__restrict__
         *reinterpret_cast<uint32_t *>(w_fp4 + blk * kBlockCodeBytes + r * 64 + (k0 % 128) / 2) = codes;
         if ((gid & 3) == 0) w_scale[blk * kBlockScaleBytes + sf_byte(r, (k0 % 128) / 32)] = (uint8_t)(X + 127);
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E, int N, int K, cudaStream_t st)
@@ -70,8 +72,7 @@ cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, in
     const long long n8 = (long long)E * N * (K / 8);
     if (n8 == 0) return cudaSuccess;
     const long long blocks = (n8 + 255) / 256;
-    pack_fp4_kernel<<<(unsigned)blocks, 256, 0, st>>>(w, w_fp4, w_scale, n8, N, K);
-    return cudaGetLastError();
+    return launch_pdl(pack_fp4_kernel, dim3((unsigned)blocks), dim3(256), 0, st, w, w_fp4, w_scale, n8, N, K);
 }
 
 // ---------------------------------------------------------------------------
@@ -109,17 +110,18 @@ __device__ __forceinline__ void quant_row_warp(const uint16_t *__restrict__ xrow
 __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
                                                        uint8_t *__restrict__ xs, int xs_stride, int T, int d)
 {
+    pdl_wait();
     const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (t >= T) return;
     quant_row_warp(x + (size_t)t * d, xq + (size_t)t * d, xs + (size_t)t * xs_stride, d, xs_stride);
+    pdl_trigger();
 }
 
 cudaError_t launch_quantize(const uint16_t *x, uint8_t *xq, uint8_t *xs, int xs_stride, int T, int d,
                             cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
-    quantize_kernel<<<(T + 7) / 8, 256, 0, st>>>(x, xq, xs, xs_stride, T, d);
-    return cudaGetLastError();
+    return launch_pdl(quantize_kernel, dim3((T + 7) / 8), dim3(256), 0, st, x, xq, xs, xs_stride, T, d);
 }
 
 // ---------------------------------------------------------------------------
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
                                                                   const float *__restrict__ bias,
                                                                   float *__restrict__ z, int T, int d, int E)
 {
+    pdl_wait();
     using namespace gate;
     constexpr int NT = WT * WE * 32;
     constexpr int CT = TW * WT;           // tokens per CTA
@@ -204,11 +207,14 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
         }
     };
 
-    float acc[TW][EW];
+    // Accumulators of adjacent experts are packed in pairs: one packed FMA
+    // (two IEEE single-precision fused multiply-adds, each rounded exactly as
+    // fmaf) updates both with the same x value, halving the instruction count.
+    float2 acc[TW][EW / 2];
 #pragma unroll
     for (int a = 0; a < TW; a++)
 #pragma unroll
-        for (int b = 0; b < EW; b++) acc[a][b] = 0.f;
+        for (int b = 0; b < EW / 2; b++) acc[a][b] = make_float2(0.f, 0.f);
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; s++) {
@@ -226,30 +232,36 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
 #pragma unroll
         for (int q = 0; q < CH / 32; q++) {
             const int i = q * 32 + lane;         // this lane's channel in the chunk
-            float xv[TW], wv[EW];
+            float2 xv[TW];
+            float2 wv[EW / 2];
 #pragma unroll
-            for (int a = 0; a < TW; a++) xv[a] = bf16_bits_to_f32(xb[a * XROW + i]);
+            for (int a = 0; a < TW; a++) {
+                const float xf = bf16_bits_to_f32(xb[a * XROW + i]);
+                xv[a] = make_float2(xf, xf);
+            }
 #pragma unroll
             for (int b = 0; b < EW; b += 4) {
                 const float4 f = *reinterpret_cast<const float4 *>(wb + i * WROW + b);
-                wv[b] = f.x; wv[b + 1] = f.y; wv[b + 2] = f.z; wv[b + 3] = f.w;
+                wv[b / 2] = make_float2(f.x, f.y);
+                wv[b / 2 + 1] = make_float2(f.z, f.w);
             }
 #pragma unroll
             for (int a = 0; a < TW; a++)
 #pragma unroll
-                for (int b = 0; b < EW; b++) acc[a][b] = fmaf(xv[a], wv[b], acc[a][b]);
+                for (int b = 0; b < EW / 2; b++) acc[a][b] = __ffma2_rn(xv[a], wv[b], acc[a][b]);
         }
     }
     cp_async_wait<0>();
 
+    float tot[TW][EW];
 #pragma unroll
     for (int a = 0; a < TW; a++)
 #pragma unroll
         for (int b = 0; b < EW; b++) {
-            float v = acc[a][b];
+            float v = (b & 1) ? acc[a][b / 2].y : acc[a][b / 2].x;
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, off);
-            acc[a][b] = v;
+            tot[a][b] = v;
         }
     // every lane holds every total; lane (a*EW+b) % 32 writes pair (a, b)
 #pragma unroll
@@ -259,11 +271,12 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
             if (((a * EW + b) & 31) != lane) continue;
             const int t = t0 + wt * TW + a, e = e0 + we * EW + b;
             if (t < T && e < E) {
-                float v = acc[a][b];
+                float v = tot[a][b];
                 if (bias) v = v + bias[e];
                 z[(size_t)t * E + e] = v;
             }
         }
+    pdl_trigger();
 }
 
 template <int TW, int EW, int WT, int WE, bool VEC_W>
@@ -276,8 +289,7 @@ static cudaError_t launch_gate_cfg(const uint16_t *x, const float *gate_w, const
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid((T + CT - 1) / CT, (E + CE - 1) / CE);
-    kern<<<grid, WT * WE * 32, smem, st>>>(x, gate_w, bias, z, T, d, E);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(WT * WE * 32), smem, st, x, gate_w, bias, z, T, d, E);
 }
 
 cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T, int d,
@@ -294,21 +306,18 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
 }
 
 // ---------------------------------------------------------------------------
-// Top-k + weights, one warp per token.  Selection order: larger logit first,
-// equal logits -> lower expert index.  s_j = fp32(sqrt(softplus(z_j))) with
-// softplus(z) = max(z, 0) + log1p(exp(-|z|)) in double; w_j = s_j / S, S the
-// fp32 sum of s_j in slot order (w_j = 1/k when S == 0).  Optionally
-// quantises the token's x row in the same pass.
+// Top-k + weights.  Selection order: larger logit first, equal logits -> lower
+// expert index.  s_j = fp32(sqrt(softplus(z_j))) with softplus(z) =
+// max(z, 0) + log1p(exp(-|z|)) in double; w_j = s_j / S, S the fp32 sum of
+// s_j in slot order (w_j = 1/k when S == 0).
+// One CTA of 8 warps per token: warp 0 selects the experts while all 8 warps
+// quantise the token's 128-channel groups of x (when xq is given), so the
+// groups' loads are in flight together rather than one after another.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ z, int32_t *__restrict__ topk_idx,
-                                                   float *__restrict__ topk_w, const uint16_t *__restrict__ x,
-                                                   uint8_t *__restrict__ xq, uint8_t *__restrict__ xs, int xs_stride,
-                                                   int T, int d, int E, int k, unsigned *status)
+__device__ __forceinline__ void topk_warp(const float *__restrict__ zt, int32_t *__restrict__ idx_out,
+                                          float *__restrict__ w_out, int E, int k, unsigned *status)
 {
-    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (t >= T) return;
     const int lane = threadIdx.x & 31;
-    const float *zt = z + (size_t)t * E;
     float v[8];
     bool bad = false;
 #pragma unroll
@@ -363,70 +372,165 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ z, 
     float S = 0.f;
     for (int j = 0; j < k; j++) S = S + __shfl_sync(0xffffffffu, s, j);
     if (lane < k) {
-        topk_idx[(size_t)t * k + lane] = my_e;
-        topk_w[(size_t)t * k + lane] = (S == 0.f) ? 1.0f / (float)k : s / S;
+        idx_out[lane] = my_e;
+        w_out[lane] = (S == 0.f) ? 1.0f / (float)k : s / S;
     }
+}
+
+constexpr int kTopkWarps = 8;
+
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float *__restrict__ z, int32_t *__restrict__ topk_idx,
+                                                               float *__restrict__ topk_w, const uint16_t *__restrict__ x,
+                                                               uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                                               int xs_stride, int T, int d, int E, int k,
+                                                               unsigned *status)
+{
+    pdl_wait();
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) topk_warp(z + (size_t)t * E, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, E, k, status);
+    if (!xq) return;
+    const uint16_t *xrow = x + (size_t)t * d;
+    uint8_t *qrow = xq + (size_t)t * d;
+    uint8_t *srow = xs + (size_t)t * xs_stride;
+    const int G = d / 128;
+    for (int g = warp; g < G; g += kTopkWarps) {
+        const int e = quant_group_warp(xrow + g * 128, qrow + g * 128);
+        if (lane == 0) srow[g] = (uint8_t)(e + 127);
+    }
+    for (int g = G + threadIdx.x; g < xs_stride; g += blockDim.x) srow[g] = 0;
+    pdl_trigger();
+}
+
+// Large batches: one warp per token (top-k, then that token's quantisation);
+// enough tokens are in flight that the per-group latency is hidden.
+__global__ void __launch_bounds__(256) topk_warp_per_token_kernel(const float *__restrict__ z,
+                                                                  int32_t *__restrict__ topk_idx,
+                                                                  float *__restrict__ topk_w,
+                                                                  const uint16_t *__restrict__ x,
+                                                                  uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                                                  int xs_stride, int T, int d, int E, int k,
+                                                                  unsigned *status)
+{
+    pdl_wait();
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    topk_warp(z + (size_t)t * E, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, E, k, status);
     if (xq) quant_row_warp(x + (size_t)t * d, xq + (size_t)t * d, xs + (size_t)t * xs_stride, d, xs_stride);
+    pdl_trigger();
 }
 
 cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const uint16_t *x, uint8_t *xq,
                         uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
-    topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(z, topk_idx, topk_w, x, xq, xs, xs_stride, T, d, E, k, status);
-    return cudaGetLastError();
+    if (T >= 2048)
+        return launch_pdl(topk_warp_per_token_kernel, dim3((T + 7) / 8), dim3(256), 0, st, z, topk_idx, topk_w, x, xq,
+                          xs, xs_stride, T, d, E, k, status);
+    return launch_pdl(topk_kernel, dim3(T), dim3(kTopkWarps * 32), 0, st, z, topk_idx, topk_w, x, xq, xs, xs_stride, T,
+                      d, E, k, status);
 }
 
 // ---------------------------------------------------------------------------
-// Dispatch plan: one CTA of 32 warps; warp w owns a contiguous chunk of the
-// pairs.  Pass 1 counts experts per chunk (warp-private rows of a shared
-// table, no atomics); a scan turns the table into each chunk's first free
-// slot per expert; pass 2 walks the chunk again in order and places every
-// pair at (its chunk's slot) + (rank among equal experts before it in the
-// 32-pair step).  The result is the unique stable order.
+// Dispatch plan (stable counting sort of the pairs by expert), no atomics on
+// positions.  The pairs are cut into C contiguous chunks, one per CTA, and
+// each CTA's chunk into 32 warp chunks.  A warp counts its pairs per expert
+// in a private row of a shared table (match_any groups equal experts of a
+// 32-pair step; each group's leader adds its size), so counting needs no
+// atomics.  With C > 1 a first kernel publishes each CTA's per-expert
+// counts; the scatter kernel (every CTA) turns all counts into global
+// offsets, gives each warp the first free slot per expert of its chunk, then
+// walks its pairs in order placing each at slot + rank among equal experts
+// earlier in the step.  The result is the unique stable order.
 // ---------------------------------------------------------------------------
 constexpr int kPlanWarps = 32;
+constexpr int kPlanPairsPerCta = 2048;
 
-__global__ void __launch_bounds__(kPlanWarps * 32) plan_kernel(const int32_t *__restrict__ topk_idx,
-                                                               int32_t *__restrict__ expert_offsets,
-                                                               int32_t *__restrict__ sorted_pair,
-                                                               int32_t *__restrict__ pair_pos,
-                                                               int32_t *__restrict__ tile_prefix, long long P, int E,
-                                                               unsigned *status)
+// Count this CTA's pairs into the warp rows cnt[warp][e]; returns nothing,
+// flags out-of-range experts (treated as expert 0 so the plan stays a bijection).
+__device__ __forceinline__ void plan_count_warps(const int32_t *__restrict__ topk_idx, int *cnt, long long pb,
+                                                 long long pe, int E, bool *bad)
 {
-    extern __shared__ int cnt[];                  // [kPlanWarps][E]
-    __shared__ int tot[257];
-    __shared__ int tiles[257];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
-    __syncthreads();
-
-    const long long chunk = (P + kPlanWarps - 1) / kPlanWarps;
-    const long long pb = warp * chunk;
-    const long long pe = (pb + chunk < P) ? pb + chunk : P;
+    const long long n = pe - pb;
+    const long long wchunk = (n + kPlanWarps - 1) / kPlanWarps;
+    const long long wb = pb + warp * wchunk;
+    const long long we = (wb + wchunk < pe) ? wb + wchunk : pe;
     int *my = cnt + warp * E;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    bool bad = false;
-
-    for (long long base = pb; base < pe; base += 32) {
+    for (long long base = wb; base < we; base += 32) {
         const long long p = base + lane;
-        const bool valid = p < pe;
+        const bool valid = p < we;
         int e = valid ? __ldg(topk_idx + p) : -1;
         if (valid && (e < 0 || e >= E)) {
-            bad = true;
+            *bad = true;
             e = 0;
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (valid && lane == __ffs(peers) - 1) my[e] += __popc(peers);
     }
+}
+
+__global__ void __launch_bounds__(kPlanWarps * 32) plan_count_kernel(const int32_t *__restrict__ topk_idx,
+                                                                     int *__restrict__ cta_counts, long long P, int E,
+                                                                     unsigned *status)
+{
+    pdl_wait();
+    extern __shared__ int cnt[];                  // [kPlanWarps][E]
+    for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    const long long pb = (long long)blockIdx.x * kPlanPairsPerCta;
+    const long long pe = (pb + kPlanPairsPerCta < P) ? pb + kPlanPairsPerCta : P;
+    bool bad = false;
+    plan_count_warps(topk_idx, cnt, pb, pe, E, &bad);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int sum = 0;
+        for (int w = 0; w < kPlanWarps; w++) sum += cnt[w * E + e];
+        cta_counts[(size_t)blockIdx.x * E + e] = sum;
+    }
+    if (bad) flag_status(status, kStatusBadData);
+    pdl_trigger();
+}
+
+// cta_counts == NULL: a single CTA covers all pairs (no count kernel needed).
+__global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int32_t *__restrict__ topk_idx,
+                                                                       const int *__restrict__ cta_counts,
+                                                                       int32_t *__restrict__ expert_offsets,
+                                                                       int32_t *__restrict__ sorted_pair,
+                                                                       int32_t *__restrict__ pair_pos,
+                                                                       int32_t *__restrict__ tile_prefix, long long P,
+                                                                       int E, unsigned *status)
+{
+    pdl_wait();
+    extern __shared__ int cnt[];                  // [kPlanWarps][E]
+    __shared__ int tot[257];                      // per-expert total, then this CTA's first slot
+    __shared__ int pre[257];                      // pairs of the expert in earlier CTAs
+    __shared__ int tiles[257];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = cta_counts ? gridDim.x : 1;
+    for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    const long long chunk = cta_counts ? kPlanPairsPerCta : P;
+    const long long pb = (long long)blockIdx.x * chunk;
+    const long long pe = (pb + chunk < P) ? pb + chunk : P;
+    bool bad = false;
+    plan_count_warps(topk_idx, cnt, pb, pe, E, &bad);
     __syncthreads();
 
-    // per-expert totals, then an exclusive scan over experts (warp 0)
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int s = 0;
-        for (int w = 0; w < kPlanWarps; w++) s += cnt[w * E + e];
-        tot[e] = s;
-        tiles[e] = (s + kTileM - 1) / kTileM;
+        int before = 0, total = 0;
+        if (cta_counts) {
+            for (int c = 0; c < C; c++) {
+                const int v = __ldg(cta_counts + (size_t)c * E + e);
+                if (c < (int)blockIdx.x) before += v;
+                total += v;
+            }
+        } else {
+            for (int w = 0; w < kPlanWarps; w++) total += cnt[w * E + e];
+        }
+        tot[e] = total;
+        pre[e] = before;
+        tiles[e] = (total + kTileM - 1) / kTileM;
     }
     __syncthreads();
     if (warp == 0) {
@@ -446,20 +550,22 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_kernel(const int32_t *__
                 }
             }
             if (e < E) {
-                expert_offsets[e] = run + inc - c;
-                if (tile_prefix) tile_prefix[e] = trun + tinc - tc;
-                tot[e] = run + inc - c;          // becomes the expert's first slot
+                if (blockIdx.x == 0) {
+                    expert_offsets[e] = run + inc - c;
+                    if (tile_prefix) tile_prefix[e] = trun + tinc - tc;
+                }
+                tot[e] = run + inc - c + pre[e];      // this CTA's first slot for expert e
             }
             run += __shfl_sync(0xffffffffu, inc, 31);
             trun += __shfl_sync(0xffffffffu, tinc, 31);
         }
-        if (lane == 0) {
+        if (lane == 0 && blockIdx.x == 0) {
             expert_offsets[E] = run;
             if (tile_prefix) tile_prefix[E] = trun;
         }
     }
     __syncthreads();
-    // chunk-local first slots
+    // each warp's first slot per expert
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = tot[e];
         for (int w = 0; w < kPlanWarps; w++) {
@@ -470,9 +576,15 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_kernel(const int32_t *__
     }
     __syncthreads();
 
-    for (long long base = pb; base < pe; base += 32) {
+    const long long n = pe - pb;
+    const long long wchunk = (n + kPlanWarps - 1) / kPlanWarps;
+    const long long wb = pb + warp * wchunk;
+    const long long we = (wb + wchunk < pe) ? wb + wchunk : pe;
+    int *my = cnt + warp * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (long long base = wb; base < we; base += 32) {
         const long long p = base + lane;
-        const bool valid = p < pe;
+        const bool valid = p < we;
         int e = valid ? __ldg(topk_idx + p) : -1;
         if (valid && (e < 0 || e >= E)) e = 0;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -486,19 +598,32 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_kernel(const int32_t *__
             pair_pos[p] = pos;
         }
     }
-    if (bad) flag_status(status, kStatusBadData);
+    if (bad && !cta_counts) flag_status(status, kStatusBadData);
+    pdl_trigger();
 }
 
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
-                        int32_t *tile_prefix, int T, int E, int k, unsigned *status, cudaStream_t st)
+                        int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st)
 {
     const long long P = (long long)T * k;
     const size_t smem = (size_t)kPlanWarps * E * sizeof(int);
-    cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const long long C = (P + kPlanPairsPerCta - 1) / kPlanPairsPerCta;
+    if (C <= 1 || !cta_counts) {
+        return launch_pdl(plan_scatter_kernel, dim3(1), dim3(kPlanWarps * 32), smem, st, topk_idx, (const int *)nullptr,
+                          expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status);
+    }
+    cudaError_t err = launch_pdl(plan_count_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
+                                 cta_counts, P, E, status);
     if (err != cudaSuccess) return err;
-    plan_kernel<<<1, kPlanWarps * 32, smem, st>>>(topk_idx, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E,
-                                                  status);
-    return cudaGetLastError();
+    return launch_pdl(plan_scatter_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
+                      (const int *)cta_counts, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status);
+}
+
+// Scratch for the multi-CTA plan: per-CTA expert counts.
+size_t plan_scratch_bytes(long long P, int E)
+{
+    const long long C = (P + kPlanPairsPerCta - 1) / kPlanPairsPerCta;
+    return C > 1 ? (size_t)C * E * sizeof(int) : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -516,6 +641,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint8_t *__restrict
                                                        uint8_t *__restrict__ xq_sorted, uint8_t *__restrict__ xs_tiles,
                                                        long long P, int d, int k)
 {
+    pdl_wait();
     const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (pos >= P) return;
     const int lane = threadIdx.x & 31;
@@ -532,6 +658,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint8_t *__restrict
     const uint32_t *ss = reinterpret_cast<const uint32_t *>(xs + (size_t)t * xs_stride);
     for (int g = lane; g < G; g += 32)
         *reinterpret_cast<uint32_t *>(xs_tiles + ((size_t)m * G + g) * kBlockScaleBytes + sf_byte(r, 0)) = __ldg(ss + g);
+    pdl_trigger();
 }
 
 cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride, const int32_t *sorted_pair,
@@ -539,9 +666,8 @@ cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride,
                             uint8_t *xq_sorted, uint8_t *xs_tiles, long long P, int d, int k, cudaStream_t st)
 {
     if (P == 0) return cudaSuccess;
-    dispatch_kernel<<<(unsigned)((P + 7) / 8), 256, 0, st>>>(xq, xs, xs_stride, sorted_pair, topk_idx, expert_offsets,
-                                                             tile_prefix, xq_sorted, xs_tiles, P, d, k);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, st, xq, xs, xs_stride, sorted_pair,
+                      topk_idx, expert_offsets, tile_prefix, xq_sorted, xs_tiles, P, d, k);
 }
 
 // ---------------------------------------------------------------------------
@@ -554,6 +680,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                                                       const float *__restrict__ topk_w, uint16_t *__restrict__ out,
                                                       int T, int d, int k)
 {
+    pdl_wait();
     const int per_tok = d / 8;
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid >= (long long)T * per_tok) return;
@@ -578,6 +705,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     o.z = pack_bf16x2(acc[4], acc[5]);
     o.w = pack_bf16x2(acc[6], acc[7]);
     reinterpret_cast<uint4 *>(out + (size_t)t * d)[c8] = o;
+    pdl_trigger();
 }
 
 cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,
@@ -585,8 +713,8 @@ cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const flo
 {
     const long long n = (long long)T * (d / 8);
     if (n == 0) return cudaSuccess;
-    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, pair_pos, topk_w, out, T, d, k);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, y, pair_pos, topk_w, out, T,
+                      d, k);
 }
 
 } // namespace fp4moe

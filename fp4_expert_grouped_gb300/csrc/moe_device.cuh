@@ -39,6 +39,22 @@ __device__ __forceinline__ uint32_t lane_id()
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel waits for the previous grid in the
+// stream (and its memory) before touching global data, and lets the next
+// grid start launching once its own work is done.  Both are no-ops when the
+// kernel was launched without the programmatic-serialisation attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)

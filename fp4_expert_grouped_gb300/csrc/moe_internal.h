@@ -60,6 +60,26 @@ inline long long max_row_tiles(long long P, int E)
     return (P + kTileM - 1) / kTileM + (P < E ? P : E);
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous grid in the stream finishes; every kernel of the library
+// waits on the previous grid (griddepcontrol.wait) before reading or writing
+// global memory, so this is safe after any predecessor.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---- launchers (kernels.cu) ----------------------------------------------
 // rows = E * N; writes the tiled layout above (N % 128 == 0, K % 128 == 0)
 cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E, int N, int K, cudaStream_t st);
@@ -71,9 +91,11 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
 // (xq/xs may be NULL).
 cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const uint16_t *x, uint8_t *xq,
                         uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st);
-// dispatch plan; tile_prefix may be NULL.
+// dispatch plan; tile_prefix may be NULL.  cta_counts: plan_scratch_bytes()
+// of scratch for large P (NULL runs the plan as one CTA whatever P).
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
-                        int32_t *tile_prefix, int T, int E, int k, unsigned *status, cudaStream_t st);
+                        int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st);
+size_t plan_scratch_bytes(long long P, int E);
 // copy every pair's quantised token row into expert order and its scales into
 // the per-tile scale layout
 cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride, const int32_t *sorted_pair,

@@ -238,6 +238,7 @@ enum {
     MOE_WS_Y,             /* bf16 [P][d], rows in expert order */
     MOE_WS_XQ_SORTED,     /* uint8 E4M3 [P][d]: row p = xq of the pair's token, expert order */
     MOE_WS_XS_TILES,      /* scales of those rows, laid out like MOE_WS_HS_TILES with d */
+    MOE_WS_PLAN_COUNTS,   /* int32 per-chunk expert counts of the dispatch plan (large batches) */
     MOE_WS_COUNT
 };
 size_t moe_workspace_layout(int T, int d, int inter, int E, int k,
