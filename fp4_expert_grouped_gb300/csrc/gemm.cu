@@ -63,8 +63,15 @@ constexpr int EPI_WARPS = 8;                   // two warps per 32-lane quarter 
 constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
-constexpr uint32_t SFA_COL = 256;
-constexpr uint32_t SFB_COL = 264;
+// Scale factors in tensor memory.  B's (8 columns) change every stage and get
+// a column set per ring stage; A's (4 columns) hold the scales of four
+// consecutive stages (one byte each), so they are copied once per group of
+// four stages into one of two slots alternating by group.  A copy therefore
+// never writes columns that MMAs still to run will read.
+constexpr uint32_t SFB_COL0 = 256;
+constexpr uint32_t SFB_COLS_PER_STAGE = 8;
+constexpr uint32_t SFA_COL0 = SFB_COL0 + STAGES * SFB_COLS_PER_STAGE;
+static_assert(SFA_COL0 + 2 * 4 <= TMEM_COLS, "tensor memory budget");
 constexpr uint32_t FULL_ARRIVALS = 1;          // the producer's expect_tx arrival; the rest is transaction bytes
 // Transaction bytes of B per stage.  The copy of packed 4-bit data spreads
 // every 8-byte group of 16 codes over a 16-byte slot (codes in the low 8
@@ -249,9 +256,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) {
                     const uint32_t sfa = sbase + OFF_SFA + stage * SFA_STAGE;
                     const uint32_t sfb = sbase + OFF_SFB + stage * SFB_STAGE;
-                    tc_cp_32x128b_warpx4(tmem + SFA_COL, sdesc_sf(sfa));
-                    tc_cp_32x128b_warpx4(tmem + SFB_COL, sdesc_sf(sfb));
-                    tc_cp_32x128b_warpx4(tmem + SFB_COL + 4, sdesc_sf(sfb + 512));
+                    const uint32_t sfa_col = tmem + SFA_COL0 + ((ks >> 2) & 1) * 4;
+                    const uint32_t sfb_col = tmem + SFB_COL0 + stage * SFB_COLS_PER_STAGE;
+                    if ((ks & 3) == 0) tc_cp_32x128b_warpx4(sfa_col, sdesc_sf(sfa));
+                    tc_cp_32x128b_warpx4(sfb_col, sdesc_sf(sfb));
+                    tc_cp_32x128b_warpx4(sfb_col + 4, sdesc_sf(sfb + 512));
                     const uint64_t adesc = sdesc_kmajor_sw128(sbase + OFF_A + stage * A_STAGE);
                     const uint64_t bdesc = sdesc_kmajor_sw128(sbase + OFF_B + stage * B_STAGE);
 #pragma unroll
@@ -259,8 +268,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // A scales: one byte per 128 channels, byte (ks % 4) of the word;
                         // B scales: one byte per 32 K-elements, byte kk of the word
                         const uint32_t idesc = IDESC_BASE | ((uint32_t)kk << 4) | ((uint32_t)(ks & 3) << 29);
-                        tc_mma_mx(tmem + ACC_COL, adesc + 2 * kk, bdesc + 2 * kk, idesc, tmem + SFA_COL,
-                                  tmem + SFB_COL, (ks | kk) != 0);
+                        tc_mma_mx(tmem + ACC_COL, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa_col, sfb_col,
+                                  (ks | kk) != 0);
                     }
                     tc_commit(&empty[stage]);
                 }
