@@ -207,6 +207,7 @@ def test_forward_tiny_all_tokens():
     (300, 256, 128, 8, 2, False),        # ragged tiles: expert groups not a multiple of 128 rows
     (257, 512, 384, 16, 4, True),        # several weight blocks and K stages, biased gate
     (64, 768, 256, 4, 4, False),         # k == E
+    (2100, 256, 128, 13, 3, True),       # large-batch gate kernel: ragged T, odd E
 ])
 def test_forward_small_shapes(T, d, inter, E, k, bias):
     w, x, gw, b, w13, w2 = small_case(T, d, inter, E, k, seed=T + d, bias=bias)
