@@ -2,8 +2,10 @@
 """MoE-layer forward throughput on GB300 (tokens/s) with its roofline fraction.
 
 One step = one moe_forward_ex call over one batch of a synthetic workload: gate
-+ top-k + FP8 quantisation, dispatch plan, dispatch copy, grouped GEMM1 (SwiGLU,
-FP8 re-quantisation), grouped GEMM2 and the combine -- every stage of the layer.
++ top-k + FP8 quantisation, dispatch plan, dispatch (rows of densely filled
+tiles copied to expert order; the rows of sparse tiles are gathered inside
+GEMM1), grouped GEMM1 (SwiGLU, FP8 re-quantisation), grouped GEMM2 and the
+combine -- every stage of the layer.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
   python bench.py --impl reference ...     # the CPU oracle on the host cores

@@ -284,7 +284,7 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     int32_t *tile_prefix = reinterpret_cast<int32_t *>(at(MOE_WS_TILE_PREFIX));
     uint8_t *hq = at(MOE_WS_HQ), *hs_tiles = at(MOE_WS_HS_TILES);
     uint16_t *y = reinterpret_cast<uint16_t *>(at(MOE_WS_Y));
-    uint8_t *xq_sorted = at(MOE_WS_XQ_SORTED), *xs_tiles = at(MOE_WS_XS_TILES);
+    uint8_t *xs_tiles = at(MOE_WS_XS_TILES);
     const int xs_stride = (int)ws.stride[MOE_WS_XS];
     const long long P = (long long)T * k;
 
@@ -300,11 +300,17 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     mark(MOE_STAGE_PLAN);
     if (e == cudaSuccess)
         e = launch_plan(topk_idx, offs, sorted_pair, pair_pos, tile_prefix,
-                        reinterpret_cast<int *>(at(MOE_WS_PLAN_COUNTS)), T, E, k, di->status, s);
+                        reinterpret_cast<int *>(at(MOE_WS_PLAN_COUNTS)), T, E, k, di->status, s, xs, xs_stride,
+                        xs_tiles, d);
+    // Dense tiles (more than 64 pairs) read A as one box of an expert-ordered
+    // copy; below 16 pairs per expert on average dense tiles are rare and the
+    // copy is skipped (every tile then gathers).  Either way the rows the MMA
+    // sees for valid pairs are the same bytes, so the output does not depend
+    // on this choice.
     mark(MOE_STAGE_DISPATCH);
-    if (e == cudaSuccess)
-        e = launch_dispatch(xq, xs, xs_stride, sorted_pair, topk_idx, offs, tile_prefix, xq_sorted, xs_tiles, P, d,
-                            k, s);
+    uint8_t *xq_sorted = P >= 16ll * E ? at(MOE_WS_XQ_SORTED) : nullptr;
+    if (e == cudaSuccess && xq_sorted)
+        e = launch_dispatch_dense(xq, sorted_pair, topk_idx, offs, xq_sorted, P, d, k, s);
     mark(MOE_STAGE_GEMM1);
     GemmArgs g;
     std::memset(&g, 0, sizeof g);
@@ -316,7 +322,11 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     g.timeout_ns = timeout_ns();
     g.num_sms = di->num_sms;
     if (e == cudaSuccess) {
-        g.a = xq_sorted;
+        g.a = xq;
+        g.a_dense = xq_sorted;
+        g.a_rows = T;
+        g.sorted_pair = sorted_pair;
+        g.k = k;
         g.a_scale_tiles = xs_tiles;
         g.b = w13_fp4;
         g.b_scale = w13_scale;
@@ -329,6 +339,8 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     mark(MOE_STAGE_GEMM2);
     if (e == cudaSuccess) {
         g.a = hq;
+        g.a_dense = nullptr;
+        g.a_rows = P;
         g.a_scale_tiles = hs_tiles;
         g.b = w2_fp4;
         g.b_scale = w2_scale;

@@ -16,9 +16,12 @@
 // the current tile's MMAs execute.
 //
 // Warp roles (320 threads):
-//   warp 0      producer: TMA tile loads of A (pair rows, E4M3; only the
-//               16-row boxes holding valid rows when a tile is sparsely
-//               filled) and B (weights, E2M1 spread to one byte per code by the
+//   warp 0      producer: GEMM1 gathers the tile's token rows of A (E4M3)
+//               with four-row TMA gathers (the dispatch to expert order
+//               happens here);
+//               GEMM2 loads A rows (hq) as TMA boxes (only the 16-row boxes
+//               holding valid rows when a tile is sparsely filled); TMA
+//               loads of B (weights, E2M1 spread to one byte per code by the
 //               copy engine; the weights are stored in contiguous 8 KB blocks)
 //               and 512-byte bulk copies of scale factors stored in the
 //               tensor cores' scale-factor order, into a 4-stage ring
@@ -72,7 +75,9 @@ constexpr uint32_t SFB_COL0 = 256;
 constexpr uint32_t SFB_COLS_PER_STAGE = 8;
 constexpr uint32_t SFA_COL0 = SFB_COL0 + STAGES * SFB_COLS_PER_STAGE;
 static_assert(SFA_COL0 + 2 * 4 <= TMEM_COLS, "tensor memory budget");
-constexpr uint32_t FULL_ARRIVALS = 1;          // the producer's expect_tx arrival; the rest is transaction bytes
+// Full-barrier arrivals: the producer's expect_tx arrival alone (every copy
+// into a stage is a TMA or bulk copy counted in transaction bytes).
+__host__ __device__ constexpr uint32_t full_arrivals(int) { return 1; }
 // Transaction bytes of B per stage.  The copy of packed 4-bit data spreads
 // every 8-byte group of 16 codes over a 16-byte slot (codes in the low 8
 // bytes, the high 8 bytes left as they were), but the barrier's transaction
@@ -113,7 +118,7 @@ __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, con
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA16,
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g, const int out_dim)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
-            mbar_init(&full[s], FULL_ARRIVALS);
+            mbar_init(&full[s], full_arrivals(MODE));
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmA16);
+        tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
@@ -172,55 +177,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // One thread issues everything: per stage one or a few TMA row boxes
-        // of A, two 8 KB blocks of B codes (spread to one byte per code in
-        // shared memory by the 4-bit copy), and three 512-byte bulk copies of
-        // scale factors already in the tensor-core order.  (Prefetching B into
-        // L2 ahead of the ring was measured and made every workload slower.)
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            const int nkt = g.K / 128;                         // K blocks per weight row block
-            const int ga = stage_groups(g.K);                   // activation scale groups per tile
-            // Where the B blocks of a tile start (first K block of each 128-row half).
-            auto b_blocks = [&](const Tile &t, long long &b0, long long &b1) {
-                int rb0, rb1;
-                if (MODE == 1) {
-                    rb0 = t.n_block * 128;
-                    rb1 = out_dim + t.n_block * 128;
-                } else {
-                    rb0 = t.n_block * BN;
-                    rb1 = rb0 + 128;
+        // Lane 0 issues the TMA and bulk copies of each stage: two 8 KB blocks
+        // of B codes (spread to one byte per code in shared memory by the 4-bit
+        // copy) and the 512-byte scale-factor blocks already in the tensor
+        // cores' order; for GEMM2 also the A rows (hq, expert order) as TMA
+        // boxes.  For GEMM1 the warp gathers the A rows -- the tile's
+        // tokens' rows of xq, i.e. the dispatch to expert order -- one TMA
+        // gather of four rows per lane, only for the groups holding valid
+        // rows; the copy engine applies the 128-byte swizzle.
+        // (Prefetching B into L2 ahead of the ring was measured and made every
+        // workload slower.)
+        uint32_t stage = 0, phase = 0;
+        const int nkt = g.K / 128;                         // K blocks per weight row block
+        const int ga = stage_groups(g.K);                   // activation scale groups per tile
+        for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+            const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb);
+            int rb0, rb1;
+            if (MODE == 1) {
+                rb0 = ti.n_block * 128;
+                rb1 = out_dim + ti.n_block * 128;
+            } else {
+                rb0 = ti.n_block * BN;
+                rb1 = rb0 + 128;
+            }
+            const long long blk0 = ((long long)ti.e * (g.N / 128) + rb0 / 128) * nkt;
+            const long long blk1 = ((long long)ti.e * (g.N / 128) + rb1 / 128) * nkt;
+            const bool small = ti.valid <= SMALL_TILE_ROWS;
+            const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
+            // GEMM1: a dense tile reads its rows as one box of the expert-ordered
+            // copy, a sparse one gathers them (four rows per TMA gather)
+            const bool dense = MODE == 1 && g.a_dense != nullptr && ti.valid > kDenseTileRows;
+            const int a_gathers = (MODE == 1 && !dense) ? (ti.valid + 3) / 4 : 0;
+            const uint32_t a_tx = (MODE == 1) ? (dense ? (uint32_t)A_STAGE : (uint32_t)a_gathers * 4 * BK)
+                                              : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
+            const uint32_t stage_tx = a_tx + B_STAGE_TX + SFA_STAGE + SFB_STAGE;
+            const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
+            // GEMM1: lane l gathers rows 4l .. 4l+3 of the tile, i.e. the xq
+            // rows of their tokens; rows past the tile's last valid row repeat
+            // its token, so every gathered row is in bounds
+            int tok[4] = {0, 0, 0, 0};
+            if (MODE == 1 && lane < a_gathers) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int r = min(4 * lane + i, ti.valid - 1);
+                    tok[i] = __ldg(g.sorted_pair + ti.row0 + r) / g.k;
                 }
-                b0 = ((long long)t.e * (g.N / 128) + rb0 / 128) * nkt;
-                b1 = ((long long)t.e * (g.N / 128) + rb1 / 128) * nkt;
-            };
-            long long tile = blockIdx.x;
-            Tile ti;
-            long long blk0 = 0, blk1 = 0;
-            for (; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-                ti = decode_tile(tile, s_tp, s_offs, E, nb);
-                b_blocks(ti, blk0, blk1);
-                // sparsely filled tiles (few rows of an expert) load only the
-                // 16-row boxes that hold valid rows
-                const bool small = ti.valid <= SMALL_TILE_ROWS;
-                const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
-                const uint32_t stage_tx =
-                    (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE) + B_STAGE_TX + SFA_STAGE + SFB_STAGE;
-                const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
-                for (int ks = 0; ks < nk; ks++) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
-                        *abort_flag = 1;
-                        break;
-                    }
-                    uint8_t *sa = smem + OFF_A + stage * A_STAGE;
-                    uint8_t *sb = smem + OFF_B + stage * B_STAGE;
-                    uint64_t *fb = &full[stage];
+            }
+            for (int ks = 0; ks < nk; ks++) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                uint8_t *sa = smem + OFF_A + stage * A_STAGE;
+                uint8_t *sb = smem + OFF_B + stage * B_STAGE;
+                uint64_t *fb = &full[stage];
+                if (lane == 0) {
                     mbar_arrive_expect_tx(fb, stage_tx);
-                    if (small) {
-                        for (int b = 0; b < a_boxes; b++)
-                            tma_load_2d(sa + b * A_SMALL_ROWS * BK, &tmA16, fb, ks * BK, ti.row0 + b * A_SMALL_ROWS);
-                    } else {
-                        tma_load_2d(sa, &tmA, fb, ks * BK, ti.row0);
+                    if (dense) tma_load_2d(sa, &tmA2, fb, ks * BK, ti.row0);
+                    if (MODE == 2) {
+                        if (small) {
+                            for (int b = 0; b < a_boxes; b++)
+                                tma_load_2d(sa + b * A_SMALL_ROWS * BK, &tmA2, fb, ks * BK, ti.row0 + b * A_SMALL_ROWS);
+                        } else {
+                            tma_load_2d(sa, &tmA, fb, ks * BK, ti.row0);
+                        }
                     }
                     tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk0 + ks));
                     tma_load_3d(sb + B_HALF, &tmB, fb, 0, 0, (int)(blk1 + ks));
@@ -228,14 +248,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint8_t *sfb = smem + OFF_SFB + stage * SFB_STAGE;
                     bulk_copy_g2s(sfb, g.b_scale + (blk0 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
                     bulk_copy_g2s(sfb + 512, g.b_scale + (blk1 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                }
+                if (MODE == 1) {
+                    __syncwarp();   // the stage's expect_tx is armed before any gather lands
+                    if (lane < a_gathers)
+                        tma_gather4(sa + lane * 4 * BK, &tmA, fb, ks * BK, tok[0], tok[1], tok[2], tok[3]);
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
         }
-        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         uint32_t stage = 0, phase = 0, acc_phase = 0;
@@ -458,9 +482,16 @@ template <int MODE>
 static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
 {
     if (a.P == 0) return cudaSuccess;
-    CUtensorMap ma, ma16, mb;
-    if (!make_map_a(&ma, a.a, a.P, a.K, gg::BM)) return cudaErrorInvalidValue;
-    if (!make_map_a(&ma16, a.a, a.P, a.K, gg::A_SMALL_ROWS)) return cudaErrorInvalidValue;
+    CUtensorMap ma, ma2, mb;
+    // GEMM1 gathers single rows of xq (box one row high); GEMM2 reads
+    // contiguous expert-ordered rows of hq.  The second A map: GEMM1 -- 128-row
+    // boxes of the dense tiles' copy (when there is one); GEMM2 -- 16-row boxes.
+    if (!make_map_a(&ma, a.a, a.a_rows, a.K, MODE == 1 ? 1 : gg::BM)) return cudaErrorInvalidValue;
+    if (MODE == 1 && a.a_dense) {
+        if (!make_map_a(&ma2, a.a_dense, a.P, a.K, gg::BM)) return cudaErrorInvalidValue;
+    } else if (!make_map_a(&ma2, a.a, a.a_rows, a.K, MODE == 1 ? 1 : gg::A_SMALL_ROWS)) {
+        return cudaErrorInvalidValue;
+    }
     if (!make_map_b(&mb, a.b, (long long)a.E * (a.N / 128) * (a.K / 128))) return cudaErrorInvalidValue;
     auto kern = gg::grouped_gemm_kernel<MODE>;
     static bool attr_set[2] = {false, false};
@@ -472,7 +503,7 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     const int nb = (MODE == 1) ? out_dim / 128 : out_dim / gg::BN;
     const long long tiles = max_row_tiles(a.P, a.E) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
-    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), gg::SMEM_BYTES, st, ma, ma16, mb, a, out_dim);
+    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), gg::SMEM_BYTES, st, ma, ma2, mb, a, out_dim);
 }
 
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm<1>(a, inter, st); }

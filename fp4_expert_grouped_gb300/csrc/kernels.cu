@@ -499,13 +499,17 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
                                                                        int32_t *__restrict__ sorted_pair,
                                                                        int32_t *__restrict__ pair_pos,
                                                                        int32_t *__restrict__ tile_prefix, long long P,
-                                                                       int E, unsigned *status)
+                                                                       int E, unsigned *status,
+                                                                       const uint8_t *__restrict__ xs, int xs_stride,
+                                                                       uint8_t *__restrict__ xs_tiles, int G4, int k)
 {
     pdl_wait();
     extern __shared__ int cnt[];                  // [kPlanWarps][E]
     __shared__ int tot[257];                      // per-expert total, then this CTA's first slot
     __shared__ int pre[257];                      // pairs of the expert in earlier CTAs
     __shared__ int tiles[257];
+    __shared__ int goff[257];                     // expert's first slot in expert order
+    __shared__ int gtp[257];                      // expert's first 128-row tile
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = cta_counts ? gridDim.x : 1;
     for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
@@ -554,6 +558,8 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
                     expert_offsets[e] = run + inc - c;
                     if (tile_prefix) tile_prefix[e] = trun + tinc - tc;
                 }
+                goff[e] = run + inc - c;
+                gtp[e] = trun + tinc - tc;
                 tot[e] = run + inc - c + pre[e];      // this CTA's first slot for expert e
             }
             run += __shfl_sync(0xffffffffu, inc, 31);
@@ -596,6 +602,17 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
         if (valid) {
             sorted_pair[pos] = (int32_t)p;
             pair_pos[p] = pos;
+            if (xs_tiles) {
+                // the pair's token scales into the GEMM's per-tile scale layout:
+                // tile m = first tile of e + local / 128, row local % 128
+                const int local = pos - goff[e];
+                const long long m = gtp[e] + local / kTileM;
+                const int r = local % kTileM;
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(xs + (size_t)(p / k) * xs_stride);
+                for (int g = 0; g < G4; g++)
+                    *reinterpret_cast<uint32_t *>(xs_tiles + ((size_t)m * G4 + g) * kBlockScaleBytes + sf_byte(r, 0)) =
+                        __ldg(src + g);
+            }
         }
     }
     if (bad && !cta_counts) flag_status(status, kStatusBadData);
@@ -603,20 +620,24 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
 }
 
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
-                        int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st)
+                        int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st,
+                        const uint8_t *xs, int xs_stride, uint8_t *xs_tiles, int d)
 {
+    const int G4 = xs_tiles ? stage_groups(d) : 0;
     const long long P = (long long)T * k;
     const size_t smem = (size_t)kPlanWarps * E * sizeof(int);
     const long long C = (P + kPlanPairsPerCta - 1) / kPlanPairsPerCta;
     if (C <= 1 || !cta_counts) {
         return launch_pdl(plan_scatter_kernel, dim3(1), dim3(kPlanWarps * 32), smem, st, topk_idx, (const int *)nullptr,
-                          expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status);
+                          expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs, xs_stride, xs_tiles, G4,
+                          k);
     }
     cudaError_t err = launch_pdl(plan_count_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                                  cta_counts, P, E, status);
     if (err != cudaSuccess) return err;
     return launch_pdl(plan_scatter_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
-                      (const int *)cta_counts, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status);
+                      (const int *)cta_counts, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs,
+                      xs_stride, xs_tiles, G4, k);
 }
 
 // Scratch for the multi-CTA plan: per-CTA expert counts.
@@ -624,50 +645,6 @@ size_t plan_scratch_bytes(long long P, int E)
 {
     const long long C = (P + kPlanPairsPerCta - 1) / kPlanPairsPerCta;
     return C > 1 ? (size_t)C * E * sizeof(int) : 0;
-}
-
-// ---------------------------------------------------------------------------
-// Dispatch copy: row `pos` of the expert-ordered activations is the quantised
-// row of token sorted_pair[pos] / k (one warp per row, 16-byte vectors).  Its
-// scales go to the per-tile layout the GEMM's scale copy reads: tile
-// m = tile_prefix[e] + local / 128, row r = local % 128, group g of four
-// 128-channel stages -> 4 bytes at (m * G + g) * 512 + sf_byte(r, 0).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) dispatch_kernel(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xs,
-                                                       int xs_stride, const int32_t *__restrict__ sorted_pair,
-                                                       const int32_t *__restrict__ topk_idx,
-                                                       const int32_t *__restrict__ expert_offsets,
-                                                       const int32_t *__restrict__ tile_prefix,
-                                                       uint8_t *__restrict__ xq_sorted, uint8_t *__restrict__ xs_tiles,
-                                                       long long P, int d, int k)
-{
-    pdl_wait();
-    const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (pos >= P) return;
-    const int lane = threadIdx.x & 31;
-    const int p = __ldg(sorted_pair + pos);
-    const int t = p / k;
-    const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)t * d);
-    uint4 *dst = reinterpret_cast<uint4 *>(xq_sorted + (size_t)pos * d);
-    for (int i = lane; i < d / 16; i += 32) dst[i] = __ldg(src + i);
-    const int e = __ldg(topk_idx + p);
-    const long long local = pos - __ldg(expert_offsets + e);
-    const long long m = __ldg(tile_prefix + e) + local / kTileM;
-    const int r = (int)(local % kTileM);
-    const int G = stage_groups(d);
-    const uint32_t *ss = reinterpret_cast<const uint32_t *>(xs + (size_t)t * xs_stride);
-    for (int g = lane; g < G; g += 32)
-        *reinterpret_cast<uint32_t *>(xs_tiles + ((size_t)m * G + g) * kBlockScaleBytes + sf_byte(r, 0)) = __ldg(ss + g);
-    pdl_trigger();
-}
-
-cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride, const int32_t *sorted_pair,
-                            const int32_t *topk_idx, const int32_t *expert_offsets, const int32_t *tile_prefix,
-                            uint8_t *xq_sorted, uint8_t *xs_tiles, long long P, int d, int k, cudaStream_t st)
-{
-    if (P == 0) return cudaSuccess;
-    return launch_pdl(dispatch_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, st, xq, xs, xs_stride, sorted_pair,
-                      topk_idx, expert_offsets, tile_prefix, xq_sorted, xs_tiles, P, d, k);
 }
 
 // ---------------------------------------------------------------------------
@@ -706,6 +683,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     o.w = pack_bf16x2(acc[6], acc[7]);
     reinterpret_cast<uint4 *>(out + (size_t)t * d)[c8] = o;
     pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+// Dense dispatch copy: row pos of the expert-ordered activations is the
+// quantised row of token sorted_pair[pos] / k, written only where pos falls in
+// a tile of more than kDenseTileRows pairs (one warp per row, 16-byte vectors).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dispatch_dense_kernel(const uint8_t *__restrict__ xq,
+                                                             const int32_t *__restrict__ sorted_pair,
+                                                             const int32_t *__restrict__ topk_idx,
+                                                             const int32_t *__restrict__ expert_offsets,
+                                                             uint8_t *__restrict__ xq_sorted, long long P, int d, int k)
+{
+    pdl_wait();
+    const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (pos < P) {
+        const int lane = threadIdx.x & 31;
+        const int p = __ldg(sorted_pair + pos);
+        const int e = __ldg(topk_idx + p);
+        const long long begin = __ldg(expert_offsets + e), count = __ldg(expert_offsets + e + 1) - begin;
+        const long long tile_first = (pos - begin) / kTileM * kTileM;
+        if (count - tile_first > kDenseTileRows) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)(p / k) * d);
+            uint4 *dst = reinterpret_cast<uint4 *>(xq_sorted + (size_t)pos * d);
+            for (int i = lane; i < d / 16; i += 32) dst[i] = __ldg(src + i);
+        }
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *sorted_pair, const int32_t *topk_idx,
+                                  const int32_t *expert_offsets, uint8_t *xq_sorted, long long P, int d, int k,
+                                  cudaStream_t st)
+{
+    if (P == 0) return cudaSuccess;
+    return launch_pdl(dispatch_dense_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, st, xq, sorted_pair,
+                      topk_idx, expert_offsets, xq_sorted, P, d, k);
 }
 
 cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,

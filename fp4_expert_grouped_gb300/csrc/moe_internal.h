@@ -93,23 +93,38 @@ cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const 
                         uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st);
 // dispatch plan; tile_prefix may be NULL.  cta_counts: plan_scratch_bytes()
 // of scratch for large P (NULL runs the plan as one CTA whatever P).
+// With xs_tiles, also writes every pair's token scales (xs [T][xs_stride],
+// d channels) into the GEMM's per-tile scale layout.
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
-                        int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st);
+                        int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st,
+                        const uint8_t *xs = nullptr, int xs_stride = 0, uint8_t *xs_tiles = nullptr, int d = 0);
 size_t plan_scratch_bytes(long long P, int E);
-// copy every pair's quantised token row into expert order and its scales into
-// the per-tile scale layout
-cudaError_t launch_dispatch(const uint8_t *xq, const uint8_t *xs, int xs_stride, const int32_t *sorted_pair,
-                            const int32_t *topk_idx, const int32_t *expert_offsets, const int32_t *tile_prefix,
-                            uint8_t *xq_sorted, uint8_t *xs_tiles, long long P, int d, int k, cudaStream_t st);
+// Tiles holding more than kDenseTileRows pairs read their A rows as one TMA
+// box from an expert-ordered copy (written by launch_dispatch_dense); the
+// others gather them from xq row by row inside GEMM1.
+constexpr int kDenseTileRows = 64;
+// copy of xq row sorted_pair[pos] / k into row pos of xq_sorted, for every pos
+// of a tile holding more than kDenseTileRows pairs
+cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *sorted_pair, const int32_t *topk_idx,
+                                  const int32_t *expert_offsets, uint8_t *xq_sorted, long long P, int d, int k,
+                                  cudaStream_t st);
 cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,
                            int d, int k, cudaStream_t st);
 
 // ---- grouped GEMMs (gemm.cu) ---------------------------------------------
 struct GemmArgs {
-    // A: pair rows in expert order, E4M3 [P][K]; scales per 128-row tile in
-    // the 512-byte order, [tiles][stage_groups(K)][512]
+    // A: GEMM1 -- quantised tokens xq [T][K], gathered in the kernel by
+    // sorted_pair (row = pair p -> token p / k); GEMM2 -- hq [P][K] rows in
+    // expert order.  Scales per 128-row tile in the 512-byte order,
+    // [tiles][stage_groups(K)][512].
     const uint8_t *a;
+    // GEMM1 only: expert-ordered copy of the A rows of the tiles holding more
+    // than kDenseTileRows pairs ([P][K]; NULL: every tile gathers)
+    const uint8_t *a_dense;
     const uint8_t *a_scale_tiles;
+    const int32_t *sorted_pair;
+    int k;
+    long long a_rows;
     // B: tiled MXFP4 weights of all experts (codes + scales), N rows, K columns
     const uint8_t *b;
     const uint8_t *b_scale;

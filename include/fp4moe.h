@@ -159,7 +159,8 @@ moe_status moe_dispatch_plan(const int32_t *topk_idx, int32_t *expert_offsets,
 
 /*
  * moe_forward -- the whole layer: gate + top-k, FP8 quantisation of x,
- * dispatch plan, grouped GEMM1 (W13, fused SwiGLU and FP8 re-quantisation of
+ * dispatch plan, grouped GEMM1 (W13; each tile gathers its tokens' FP8 rows,
+ * the dispatch; fused SwiGLU and FP8 re-quantisation of
  * h with one power-of-two scale per 128 channels), grouped GEMM2 (W2, output
  * rounded to bf16) and the combine out_t = bf16(fp32 fused multiply-add chain
  * over slots j = 0..k-1 of w_j * y_j).
@@ -196,9 +197,9 @@ typedef struct moe_forward_opts {
 enum {
     MOE_STAGE_GATE = 0,   /* fixed-order fp32 gate logits */
     MOE_STAGE_TOPK,       /* top-k, weights and FP8 quantisation of x */
-    MOE_STAGE_PLAN,       /* dispatch plan (stable counting sort) */
-    MOE_STAGE_DISPATCH,   /* copy of every pair's FP8 token row into expert order */
-    MOE_STAGE_GEMM1,      /* grouped W13 GEMM + SwiGLU + FP8 re-quantisation */
+    MOE_STAGE_PLAN,       /* dispatch plan (stable counting sort) + scale tiles */
+    MOE_STAGE_DISPATCH,   /* copy of the FP8 token rows of densely filled tiles into expert order */
+    MOE_STAGE_GEMM1,      /* grouped W13 GEMM (gathers the rows of sparse tiles) + SwiGLU + FP8 */
     MOE_STAGE_GEMM2,      /* grouped W2 GEMM, bf16 output */
     MOE_STAGE_COMBINE,    /* slot-order weighted combine */
     MOE_STAGE_COUNT
@@ -236,8 +237,11 @@ enum {
                              (m * ceil(inter/512) + g) * 512, the byte of row r
                              and group 4g + j at (r % 32) * 16 + (r / 32) * 4 + j */
     MOE_WS_Y,             /* bf16 [P][d], rows in expert order */
-    MOE_WS_XQ_SORTED,     /* uint8 E4M3 [P][d]: row p = xq of the pair's token, expert order */
-    MOE_WS_XS_TILES,      /* scales of those rows, laid out like MOE_WS_HS_TILES with d */
+    MOE_WS_XQ_SORTED,     /* uint8 E4M3 [P][d]: row p = xq of the pair's token, expert order;
+                             written only for the rows of tiles holding more than 64 pairs
+                             (the others are gathered from xq inside GEMM1) */
+    MOE_WS_XS_TILES,      /* scales of the expert-ordered pair rows (their tokens' xs), laid
+                             out like MOE_WS_HS_TILES with d */
     MOE_WS_PLAN_COUNTS,   /* int32 per-chunk expert counts of the dispatch plan (large batches) */
     MOE_WS_COUNT
 };

@@ -353,3 +353,42 @@ def test_workspace_intermediates_tiny():
         deq = (deq * np.exp2(hs.astype(np.float64) - 127)[:, None]).reshape(-1)
         h, _, _, _ = oracle.expert_pair(oq[t], os_[t], ridx[t, j], f13, s13, f2, s2)
         assert np.linalg.norm(deq - h) <= 0.05 * np.linalg.norm(h) + 1e-30
+
+
+def test_dense_copy_and_gathered_tiles_agree():
+    """Tiles of more than 64 pairs read their A rows from the expert-ordered
+    copy, the others gather them from xq inside GEMM1, and a batch of under 16
+    pairs per expert gathers every tile.  The copied rows are xq bit for bit,
+    the layer is within tolerance of the oracle, and a token's output is the
+    same bits whichever way its tile was loaded."""
+    T, d, inter, E, k = 700, 256, 128, 8, 2
+    w, x, gw, b, w13, w2 = small_case(T, d, inter, E, k, seed=77, bias=True)
+    out, pk = run_small_forward(w, x, gw, b, w13, w2)
+    bd = None if b is None else b.to(DEV)
+    ws = layer().workspace(T, d, inter, E, k)
+    again = layer().forward(x.to(DEV), gw.to(DEV), pk, k, gate_bias=bd, ws=ws)
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+    xb = inputs.bf16_bits(x)
+    oq, _ = oracle.quant_act(xb)
+    ridx, _ = oracle.route(xb, gw.numpy(), k, None if b is None else b.numpy())
+    offs, sp, _ = oracle.dispatch_plan(ridx, E)
+    c = capi()
+    _, off, _ = c.moe_workspace_layout(T, d, inter, E, k)
+    xqs = ws.cpu().numpy()[off[c.MOE_WS_XQ_SORTED]:][:T * k * d].reshape(T * k, d)
+    dense = sparse = 0
+    for e in range(E):
+        n = int(offs[e + 1] - offs[e])
+        for t0 in range(0, n, 128):
+            rows = min(128, n - t0)
+            if rows <= 64:
+                sparse += 1
+                continue
+            dense += 1
+            for r in range(rows):
+                pos = offs[e] + t0 + r
+                assert np.array_equal(xqs[pos], oq[sp[pos] // k]), (e, t0, r)
+    assert dense >= 2 and sparse >= 2
+    for sl in (slice(0, 40), slice(650, 700), slice(123, 124)):
+        part = layer().forward(x[sl].contiguous().to(DEV), gw.to(DEV), pk, k, gate_bias=bd)
+        assert torch.equal(part.view(torch.int16), out[sl].view(torch.int16))
+    assert c.moe_get_device_status() == 0
