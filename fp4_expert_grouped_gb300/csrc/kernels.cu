@@ -131,12 +131,10 @@ cudaError_t launch_quantize(const uint16_t *x, uint8_t *xq, uint8_t *xs, int xs_
 // owns a TW x EW tile of (token, expert) pairs, every lane accumulates its
 // channel subsequence for all of them, and the final xor-butterfly adds
 // exactly the tree's pairs (each add is commutative, so every lane ends with
-// the tree's total).  Chunks of 128 channels of x and gate_w are staged in
-// shared memory through a cp.async pipeline.
+// the tree's total).  Chunks of CH (128 or 256) channels of x and gate_w are
+// staged in shared memory through a STAGES-deep cp.async pipeline.
 // ---------------------------------------------------------------------------
 namespace gate {
-constexpr int CH = 128;
-constexpr int STAGES = 4;
 
 __device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, bool pred)
 {
@@ -153,7 +151,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 } // namespace gate
 
-template <int TW, int EW, int WT, int WE, bool VEC_W>
+template <int TW, int EW, int WT, int WE, bool VEC_W, int CH, int STAGES>
 __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t *__restrict__ x,
                                                                   const float *__restrict__ gate_w,
                                                                   const float *__restrict__ bias,
@@ -167,6 +165,7 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
     constexpr int WROW = CE + 4;          // padded gate_w row in shared memory (floats)
     constexpr int XROW = CH + 8;          // padded x row (bf16 elements)
     static_assert(CE % 4 == 0, "expert tile must be a multiple of 4");
+    static_assert(CH % 32 == 0, "channel chunk must be a multiple of 32");
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint16_t *xs_ = reinterpret_cast<uint16_t *>(smem_raw);                       // [STAGES][CT][XROW]
@@ -279,13 +278,14 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
     pdl_trigger();
 }
 
-template <int TW, int EW, int WT, int WE, bool VEC_W>
+template <int TW, int EW, int WT, int WE, bool VEC_W, int CH = 128, int STAGES = 4>
 static cudaError_t launch_gate_cfg(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T, int d,
                                    int E, cudaStream_t st)
 {
     constexpr int CT = TW * WT, CE = EW * WE;
-    const size_t smem = (size_t)gate::STAGES * (CT * (gate::CH + 8) * 2 + gate::CH * (CE + 4) * 4);
-    auto kern = gate_logits_kernel<TW, EW, WT, WE, VEC_W>;
+    if (d % CH) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)STAGES * (CT * (CH + 8) * 2 + CH * (CE + 4) * 4);
+    auto kern = gate_logits_kernel<TW, EW, WT, WE, VEC_W, CH, STAGES>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid((T + CT - 1) / CT, (E + CE - 1) / CE);
@@ -296,13 +296,21 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
                                int E, cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
-    const bool vec = (E % 4) == 0;
-    if (T >= 2048) {
-        return vec ? launch_gate_cfg<8, 16, 4, 2, true>(x, gate_w, bias, z, T, d, E, st)
-                   : launch_gate_cfg<8, 16, 4, 2, false>(x, gate_w, bias, z, T, d, E, st);
+    // Tile shapes measured at E = 256 (all give the same bits): a 48 x 32
+    // (token x expert) CTA tile of twelve 8 x 16 warp tiles from 1536 tokens
+    // on, 24 x 16 from 384, 16 x 8 below; 256-channel chunks (fewer block
+    // barriers) where d allows.  E not a multiple of 4 loads gate_w by words.
+    if (E % 4) {
+        return T >= 2048 ? launch_gate_cfg<8, 16, 4, 2, false>(x, gate_w, bias, z, T, d, E, st)
+                         : launch_gate_cfg<4, 8, 4, 1, false>(x, gate_w, bias, z, T, d, E, st);
     }
-    return vec ? launch_gate_cfg<4, 8, 4, 1, true>(x, gate_w, bias, z, T, d, E, st)
-               : launch_gate_cfg<4, 8, 4, 1, false>(x, gate_w, bias, z, T, d, E, st);
+    if (d % 256) {
+        return T >= 1536 ? launch_gate_cfg<8, 16, 6, 2, true>(x, gate_w, bias, z, T, d, E, st)
+                         : launch_gate_cfg<4, 8, 4, 1, true>(x, gate_w, bias, z, T, d, E, st);
+    }
+    if (T >= 1536) return launch_gate_cfg<8, 16, 6, 2, true, 256, 2>(x, gate_w, bias, z, T, d, E, st);
+    if (T >= 384) return launch_gate_cfg<4, 16, 6, 1, true, 256, 3>(x, gate_w, bias, z, T, d, E, st);
+    return launch_gate_cfg<4, 8, 4, 1, true, 256, 3>(x, gate_w, bias, z, T, d, E, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -141,6 +141,10 @@ def test_quantize_act_bitexact():
     (64, 512, 8, 8, False, False),        # k == E
     (96, 768, 256, 6, False, True),
     (50, 384, 13, 3, True, True),         # E not a multiple of 4
+    (2333, 7168, 256, 8, False, True),    # large-batch gate tile at prefill width, ragged T
+    (700, 1280, 64, 6, False, True),      # mid-batch gate tile
+    (1600, 640, 32, 4, True, False),      # large batch, d not a multiple of 256 (128-channel chunks)
+    (40, 384, 16, 4, False, False),       # small batch, 128-channel chunks
 ])
 def test_route_bitexact(T, d, E, k, ties, bias):
     rng = np.random.default_rng(T * 31 + E)
