@@ -116,7 +116,10 @@ __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, con
     return t;
 }
 
-template <int MODE>
+// DENSE (GEMM1 only): some tiles read A from the expert-ordered copy.  A
+// separate instantiation keeps that path's code out of the gather-only
+// producer, whose loop is sensitive to its size when the GEMM streams weights.
+template <int MODE, bool DENSE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g, const int out_dim)
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
             // GEMM1: a dense tile reads its rows as one box of the expert-ordered
             // copy, a sparse one gathers them (four rows per TMA gather)
-            const bool dense = MODE == 1 && g.a_dense != nullptr && ti.valid > kDenseTileRows;
+            const bool dense = DENSE && ti.valid > kDenseTileRows;
             const int a_gathers = (MODE == 1 && !dense) ? (ti.valid + 3) / 4 : 0;
             const uint32_t a_tx = (MODE == 1) ? (dense ? (uint32_t)A_STAGE : (uint32_t)a_gathers * 4 * BK)
                                               : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
@@ -493,13 +496,12 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
         return cudaErrorInvalidValue;
     }
     if (!make_map_b(&mb, a.b, (long long)a.E * (a.N / 128) * (a.K / 128))) return cudaErrorInvalidValue;
-    auto kern = gg::grouped_gemm_kernel<MODE>;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[MODE - 1]) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
-        if (err != cudaSuccess) return err;
-        attr_set[MODE - 1] = true;
+    auto kern = gg::grouped_gemm_kernel<MODE, false>;
+    if constexpr (MODE == 1) {
+        if (a.a_dense) kern = gg::grouped_gemm_kernel<1, true>;
     }
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
     const int nb = (MODE == 1) ? out_dim / 128 : out_dim / gg::BN;
     const long long tiles = max_row_tiles(a.P, a.E) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
