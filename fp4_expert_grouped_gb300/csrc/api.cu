@@ -99,7 +99,7 @@ bool workspace_layout(const Shapes &s, Workspace *ws)
     if (!layer_shape_ok(s.T, s.d, s.inter, s.E, s.k)) return false;
     const size_t T = s.T, d = s.d, I = s.inter, E = s.E, k = s.k, P = T * k;
     const size_t xs_stride = scale_row_stride(s.d);
-    const size_t tiles = (size_t)max_row_tiles((long long)P, s.E);
+    const size_t tiles = (size_t)max_row_tiles((long long)P, s.E, gemm_tile_rows((long long)P, s.E));
     const size_t xs_tiles = tiles * stage_groups(s.d) * kBlockScaleBytes;
     const size_t hs_tiles = tiles * stage_groups(s.inter) * kBlockScaleBytes;
     size_t bytes[MOE_WS_COUNT], stride[MOE_WS_COUNT];
@@ -301,7 +301,7 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     if (e == cudaSuccess)
         e = launch_plan(topk_idx, offs, sorted_pair, pair_pos, tile_prefix,
                         reinterpret_cast<int *>(at(MOE_WS_PLAN_COUNTS)), T, E, k, di->status, s, xs, xs_stride,
-                        xs_tiles, d);
+                        xs_tiles, d, gemm_tile_rows(P, E));
     // Dense tiles (more than 64 pairs) read A as one box of an expert-ordered
     // copy; below 16 pairs per expert on average dense tiles are rare and the
     // copy is skipped (every tile then gathers).  Either way the rows the MMA
@@ -321,6 +321,7 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     g.status = di->status;
     g.timeout_ns = timeout_ns();
     g.num_sms = di->num_sms;
+    g.tile_rows = gemm_tile_rows(P, E);
     if (e == cudaSuccess) {
         g.a = xq;
         g.a_dense = xq_sorted;

@@ -43,27 +43,38 @@ namespace gg {
 constexpr int BM = kTileM;
 constexpr int BN = kTileN;
 constexpr int BK = kTileK;
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * BK;          // 16 KB of E4M3
-constexpr int B_STAGE = BN * BK;          // 32 KB: 256 rows x 128 codes, one byte per code in shared memory
-constexpr int B_HALF = B_STAGE / 2;
 constexpr int A_SMALL_ROWS = 16;          // row box used when a tile holds <= SMALL_TILE_ROWS valid rows
 constexpr int SMALL_TILE_ROWS = 64;
 constexpr int SFA_STAGE = 512;            // 128 rows x 4 bytes
 constexpr int SFB_STAGE = 1024;           // 256 rows x 4 bytes
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-constexpr int OFF_AMAX = OFF_SFB + STAGES * SFB_STAGE;          // [2 tile parities][2 halves][128 rows] fp32
-constexpr int OFF_BAR = OFF_AMAX + 2 * 2 * BM * 4;
-constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2 + 4) * 8;   // + one amax-exchange barrier per lane quarter
-constexpr int OFF_PLAN = OFF_MISC + 16;
+constexpr int B_STAGE = BN * BK;          // 32 KB: 256 rows x 128 codes, one byte per code in shared memory
+constexpr int B_HALF = B_STAGE / 2;
 constexpr int PLAN_INTS = 260;
-constexpr int SMEM_USED = OFF_PLAN + 2 * PLAN_INTS * 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
-constexpr int EPI_WARPS = 8;                   // two warps per 32-lane quarter of tensor memory
+constexpr int EPI_WARPS = 8;              // two warps per 32-lane quarter of tensor memory
 constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
+
+// Shared-memory layout per tile size TR (pair rows per tile).  TR = 128: a
+// 4-stage ring of 48 KB stages (A 16 KB, B 32 KB).  TR = 16: A slots of 2 KB
+// and a 6-stage ring (50% more weight bytes in flight).  The MMA always reads
+// 128 A rows (16 KB) from a slot's start; with 2 KB slots the rows past 16
+// come from whatever follows the slot in shared memory and only feed
+// accumulator rows that are discarded.  The A slots therefore come first.
+template <int TR>
+struct Cfg {
+    static constexpr int STAGES = TR == 16 ? 6 : 4;
+    static constexpr int A_STAGE = TR * BK;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+    static constexpr int OFF_AMAX = OFF_SFB + STAGES * SFB_STAGE;          // [2 tile parities][2 halves][128 rows] fp32
+    static constexpr int OFF_BAR = OFF_AMAX + 2 * 2 * BM * 4;
+    static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2 + 4) * 8;   // + one amax-exchange barrier per lane quarter
+    static constexpr int OFF_PLAN = OFF_MISC + 16;
+    static constexpr int SMEM_USED = OFF_PLAN + 2 * PLAN_INTS * 4;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
+        static_assert((STAGES - 1) * A_STAGE + BM * BK <= SMEM_USED, "MMA A reads stay in shared memory");
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 // Scale factors in tensor memory.  B's (8 columns) change every stage and get
@@ -73,7 +84,7 @@ constexpr uint32_t ACC_COL = 0;
 // never writes columns that MMAs still to run will read.
 constexpr uint32_t SFB_COL0 = 256;
 constexpr uint32_t SFB_COLS_PER_STAGE = 8;
-constexpr uint32_t SFA_COL0 = SFB_COL0 + STAGES * SFB_COLS_PER_STAGE;
+constexpr uint32_t SFA_COL0 = SFB_COL0 + 6 * SFB_COLS_PER_STAGE;   // after the deepest ring's B columns
 static_assert(SFA_COL0 + 2 * 4 <= TMEM_COLS, "tensor memory budget");
 // Full-barrier arrivals: the producer's expect_tx arrival alone (every copy
 // into a stage is a TMA or bulk copy counted in transaction bytes).
@@ -89,13 +100,12 @@ constexpr uint32_t B_STAGE_TX = B_STAGE / 2;
 constexpr uint32_t IDESC_BASE = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
                                 ((uint32_t)(BM >> 4) << 24);
 
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Tile {
-    int e, m_tile, n_block, row0, valid;   // m_tile: index of the 128-row tile among all experts' tiles
+    int e, m_tile, n_block, row0, valid;   // m_tile: index of the row tile among all experts' tiles
 };
 
-__device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, const int *s_offs, int E, int nb)
+__device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, const int *s_offs, int E, int nb, int TR)
 {
     int lo = 0, hi = E;
     while (lo < hi) {
@@ -110,20 +120,26 @@ __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, con
     const int m_block = (int)(local % mb);
     t.m_tile = s_tp[lo] + m_block;
     t.n_block = (int)(local / mb);
-    t.row0 = s_offs[lo] + m_block * BM;
+    t.row0 = s_offs[lo] + m_block * TR;
     const int rem = s_offs[lo + 1] - t.row0;
-    t.valid = rem < BM ? rem : BM;
+    t.valid = rem < TR ? rem : TR;
     return t;
 }
 
 // DENSE (GEMM1 only): some tiles read A from the expert-ordered copy.  A
 // separate instantiation keeps that path's code out of the gather-only
 // producer, whose loop is sensitive to its size when the GEMM streams weights.
-template <int MODE, bool DENSE>
+// TR: pair rows per tile (16 or 128).
+template <int MODE, bool DENSE, int TR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g, const int out_dim)
 {
+    using C = Cfg<TR>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int A_STAGE = C::A_STAGE;
+    constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_SFA = C::OFF_SFA, OFF_SFB = C::OFF_SFB;
+    constexpr int OFF_AMAX = C::OFF_AMAX, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC, OFF_PLAN = C::OFF_PLAN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
@@ -147,7 +163,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, EPI_WARPS * 32);
+        // 16-row tiles: only the two epilogue warps of lane quarter 0 hold rows
+        mbar_init(acc_empty, TR == 16 ? 64 : EPI_WARPS * 32);
         for (int i = 0; i < 4; i++) mbar_init(&xbar[i], 64);
         *abort_flag = 0;
         mbar_fence_init();
@@ -194,7 +211,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int nkt = g.K / 128;                         // K blocks per weight row block
         const int ga = stage_groups(g.K);                   // activation scale groups per tile
         for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-            const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb);
+            const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb, TR);
             int rb0, rb1;
             if (MODE == 1) {
                 rb0 = ti.n_block * 128;
@@ -205,7 +222,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const long long blk0 = ((long long)ti.e * (g.N / 128) + rb0 / 128) * nkt;
             const long long blk1 = ((long long)ti.e * (g.N / 128) + rb1 / 128) * nkt;
-            const bool small = ti.valid <= SMALL_TILE_ROWS;
+            const bool small = TR == 16 || ti.valid <= SMALL_TILE_ROWS;   // 16-row tiles: always 16-row boxes
             const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
             // GEMM1: a dense tile reads its rows as one box of the expert-ordered
             // copy, a sparse one gathers them (four rows per TMA gather)
@@ -325,8 +342,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = q * 32 + lane;               // accumulator row = pair row in the tile
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL;
         uint32_t acc_phase = 0, tpar = 0;
-        for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-            const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb);
+        // 16-row tiles have no rows in lane quarters 1-3
+        for (long long tile = blockIdx.x; (TR == 128 || q == 0) && tile < total_tiles && !*abort_flag;
+             tile += gridDim.x) {
+            const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb, TR);
             if (!mbar_wait(acc_full, acc_phase, tmo, abort_flag)) {
                 *abort_flag = 1;
                 break;
@@ -496,16 +515,26 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
         return cudaErrorInvalidValue;
     }
     if (!make_map_b(&mb, a.b, (long long)a.E * (a.N / 128) * (a.K / 128))) return cudaErrorInvalidValue;
-    auto kern = gg::grouped_gemm_kernel<MODE, false>;
-    if constexpr (MODE == 1) {
-        if (a.a_dense) kern = gg::grouped_gemm_kernel<1, true>;
+    auto kern = gg::grouped_gemm_kernel<MODE, false, 128>;
+    int smem = gg::Cfg<128>::SMEM_BYTES;
+    if (a.tile_rows == 16) {
+        kern = gg::grouped_gemm_kernel<MODE, false, 16>;
+        smem = gg::Cfg<16>::SMEM_BYTES;
+    } else if (a.tile_rows != 128) {
+        return cudaErrorInvalidValue;
     }
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
+    if constexpr (MODE == 1) {
+        if (a.a_dense) {
+            if (a.tile_rows != 128) return cudaErrorInvalidValue;
+            kern = gg::grouped_gemm_kernel<1, true, 128>;
+        }
+    }
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     const int nb = (MODE == 1) ? out_dim / 128 : out_dim / gg::BN;
-    const long long tiles = max_row_tiles(a.P, a.E) * nb;
+    const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
-    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), gg::SMEM_BYTES, st, ma, ma2, mb, a, out_dim);
+    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), smem, st, ma, ma2, mb, a, out_dim);
 }
 
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm<1>(a, inter, st); }

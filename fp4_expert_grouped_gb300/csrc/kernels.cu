@@ -509,7 +509,8 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
                                                                        int32_t *__restrict__ tile_prefix, long long P,
                                                                        int E, unsigned *status,
                                                                        const uint8_t *__restrict__ xs, int xs_stride,
-                                                                       uint8_t *__restrict__ xs_tiles, int G4, int k)
+                                                                       uint8_t *__restrict__ xs_tiles, int G4, int k,
+                                                                       int tile_rows)
 {
     pdl_wait();
     extern __shared__ int cnt[];                  // [kPlanWarps][E]
@@ -517,7 +518,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
     __shared__ int pre[257];                      // pairs of the expert in earlier CTAs
     __shared__ int tiles[257];
     __shared__ int goff[257];                     // expert's first slot in expert order
-    __shared__ int gtp[257];                      // expert's first 128-row tile
+    __shared__ int gtp[257];                      // expert's first row tile (tile_rows pairs each)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = cta_counts ? gridDim.x : 1;
     for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
@@ -542,7 +543,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
         }
         tot[e] = total;
         pre[e] = before;
-        tiles[e] = (total + kTileM - 1) / kTileM;
+        tiles[e] = (total + tile_rows - 1) / tile_rows;
     }
     __syncthreads();
     if (warp == 0) {
@@ -612,10 +613,10 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
             pair_pos[p] = pos;
             if (xs_tiles) {
                 // the pair's token scales into the GEMM's per-tile scale layout:
-                // tile m = first tile of e + local / 128, row local % 128
+                // tile m = first tile of e + local / tile_rows, row local % tile_rows
                 const int local = pos - goff[e];
-                const long long m = gtp[e] + local / kTileM;
-                const int r = local % kTileM;
+                const long long m = gtp[e] + local / tile_rows;
+                const int r = local % tile_rows;
                 const uint32_t *src = reinterpret_cast<const uint32_t *>(xs + (size_t)(p / k) * xs_stride);
                 for (int g = 0; g < G4; g++)
                     *reinterpret_cast<uint32_t *>(xs_tiles + ((size_t)m * G4 + g) * kBlockScaleBytes + sf_byte(r, 0)) =
@@ -629,7 +630,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
 
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
                         int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st,
-                        const uint8_t *xs, int xs_stride, uint8_t *xs_tiles, int d)
+                        const uint8_t *xs, int xs_stride, uint8_t *xs_tiles, int d, int tile_rows)
 {
     const int G4 = xs_tiles ? stage_groups(d) : 0;
     const long long P = (long long)T * k;
@@ -638,14 +639,14 @@ cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_
     if (C <= 1 || !cta_counts) {
         return launch_pdl(plan_scatter_kernel, dim3(1), dim3(kPlanWarps * 32), smem, st, topk_idx, (const int *)nullptr,
                           expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs, xs_stride, xs_tiles, G4,
-                          k);
+                          k, tile_rows);
     }
     cudaError_t err = launch_pdl(plan_count_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                                  cta_counts, P, E, status);
     if (err != cudaSuccess) return err;
     return launch_pdl(plan_scatter_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                       (const int *)cta_counts, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs,
-                      xs_stride, xs_tiles, G4, k);
+                      xs_stride, xs_tiles, G4, k, tile_rows);
 }
 
 // Scratch for the multi-CTA plan: per-CTA expert counts.

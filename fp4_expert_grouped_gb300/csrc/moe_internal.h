@@ -55,9 +55,19 @@ bool workspace_layout(const Shapes &s, Workspace *ws);
 inline int scale_row_stride(int channels) { return ((channels / 128) + 3) / 4 * 4; }
 
 // upper bound on the number of 128-row tiles of the expert-ordered pairs
-inline long long max_row_tiles(long long P, int E)
+// Pair rows per GEMM row tile: 16 for batches averaging at most 8 pairs per
+// expert, 128 otherwise.  A small batch's tiles hold a few rows each, and the
+// shared memory a 128-row A slot takes is better spent on a deeper ring of
+// weight stages (the GEMMs then stream weights at ~90% of HBM bandwidth
+// instead of ~80%).  The MMA still computes 128 rows; rows past the tile's
+// own are discarded, so a row's result does not depend on the tile size.
+__host__ __device__ inline int gemm_tile_rows(long long P, int E) { return P <= 8LL * E ? 16 : kTileM; }
+
+// Upper bound of the row tiles of all experts: every expert's last tile may
+// be partial.
+inline long long max_row_tiles(long long P, int E, int tile_rows)
 {
-    return (P + kTileM - 1) / kTileM + (P < E ? P : E);
+    return (P + tile_rows - 1) / tile_rows + (P < E ? P : E);
 }
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled
@@ -97,7 +107,8 @@ cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const 
 // d channels) into the GEMM's per-tile scale layout.
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
                         int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st,
-                        const uint8_t *xs = nullptr, int xs_stride = 0, uint8_t *xs_tiles = nullptr, int d = 0);
+                        const uint8_t *xs = nullptr, int xs_stride = 0, uint8_t *xs_tiles = nullptr, int d = 0,
+                        int tile_rows = kTileM);
 size_t plan_scratch_bytes(long long P, int E);
 // Tiles holding more than kDenseTileRows pairs read their A rows as one TMA
 // box from an expert-ordered copy (written by launch_dispatch_dense); the
@@ -117,6 +128,7 @@ struct GemmArgs {
     // sorted_pair (row = pair p -> token p / k); GEMM2 -- hq [P][K] rows in
     // expert order.  Scales per 128-row tile in the 512-byte order,
     // [tiles][stage_groups(K)][512].
+    int tile_rows;                   // gemm_tile_rows(P, E): 16 or 128 pair rows per tile
     const uint8_t *a;
     // GEMM1 only: expert-ordered copy of the A rows of the tiles holding more
     // than kDenseTileRows pairs ([P][K]; NULL: every tile gathers)

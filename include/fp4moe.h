@@ -230,11 +230,12 @@ enum {
     MOE_WS_EXPERT_OFFSETS,/* int32 [E+1] */
     MOE_WS_SORTED_PAIR,   /* int32 [P] */
     MOE_WS_PAIR_POS,      /* int32 [P] */
-    MOE_WS_TILE_PREFIX,   /* int32 [E+1] running count of 128-row tiles */
+    MOE_WS_TILE_PREFIX,   /* int32 [E+1] running count of the GEMMs' row tiles of R pairs each:
+                             R = 16 when T*k <= 8*E (small batches), else 128 */
     MOE_WS_HQ,            /* uint8 E4M3 [P][inter], rows in expert order */
-    MOE_WS_HS_TILES,      /* uint8 scales of hq per 128-row tile m and group g
-                             of four 128-channel groups: 512-byte blocks at
-                             (m * ceil(inter/512) + g) * 512, the byte of row r
+    MOE_WS_HS_TILES,      /* uint8 scales of hq per row tile m (R rows, as above) and
+                             group g of four 128-channel groups: 512-byte blocks
+                             at (m * ceil(inter/512) + g) * 512, the byte of row r
                              and group 4g + j at (r % 32) * 16 + (r / 32) * 4 + j */
     MOE_WS_Y,             /* bf16 [P][d], rows in expert order */
     MOE_WS_XQ_SORTED,     /* uint8 E4M3 [P][d]: row p = xq of the pair's token, expert order;

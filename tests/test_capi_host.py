@@ -103,7 +103,8 @@ def test_workspace_layout(capi):
         assert total == capi.moe_workspace_size(T, d, inter, E, k) > 0
         P = T * k
         xs = ((d // 128) + 3) // 4 * 4
-        tiles = (P + 127) // 128 + min(P, E)
+        R = 16 if P <= 8 * E else 128          # pair rows per GEMM row tile
+        tiles = (P + R - 1) // R + min(P, E)
         gx, gh = (d // 128 + 3) // 4, (inter // 128 + 3) // 4
         chunks = (P + 2047) // 2048
         sizes = [T * d, T * xs, T * E * 4, P * 4, P * 4, (E + 1) * 4, P * 4, P * 4, (E + 1) * 4,

@@ -212,6 +212,8 @@ def test_forward_tiny_all_tokens():
     (257, 512, 384, 16, 4, True),        # several weight blocks and K stages, biased gate
     (64, 768, 256, 4, 4, False),         # k == E
     (2100, 256, 128, 13, 3, True),       # large-batch gate kernel: ragged T, odd E
+    (48, 256, 128, 16, 2, True),         # 16-row tiles: experts of 16 and 17 pairs (a 1-row tail tile), empty experts
+    (60, 512, 128, 8, 1, True),          # 16-row tiles, k = 1, one expert spanning two tiles
 ])
 def test_forward_small_shapes(T, d, inter, E, k, bias):
     w, x, gw, b, w13, w2 = small_case(T, d, inter, E, k, seed=T + d, bias=bias)
@@ -344,14 +346,15 @@ def test_workspace_intermediates_tiny():
     f2, s2 = oracle.pack_fp4(w2.numpy())
     hq = wsn[off[c.MOE_WS_HQ]:][:w.P * w.inter].reshape(w.P, w.inter)
     tp = wsn[off[c.MOE_WS_TILE_PREFIX]:][:4 * (w.E + 1)].view(np.int32)
-    assert np.array_equal(tp, np.concatenate([[0], np.cumsum((np.diff(offs) + 127) // 128)]))
+    R = 16 if w.P <= 8 * w.E else 128          # pair rows per GEMM row tile
+    assert np.array_equal(tp, np.concatenate([[0], np.cumsum((np.diff(offs) + R - 1) // R)]))
     hs_tiles = wsn[off[c.MOE_WS_HS_TILES]:]
     GH = (w.inter // 128 + 3) // 4
     for pos in range(w.P):
         t, j = divmod(int(sp[pos]), w.k)
         e = ridx[t, j]
         local = pos - offs[e]
-        m, r = tp[e] + local // 128, local % 128
+        m, r = tp[e] + local // R, local % R
         hs = np.array([hs_tiles[(m * GH + nb // 4) * 512 + sf_byte(r, nb % 4)] for nb in range(w.inter // 128)])
         deq = torch.from_numpy(hq[pos].copy()).view(torch.float8_e4m3fn).double().numpy().reshape(-1, 128)
         deq = (deq * np.exp2(hs.astype(np.float64) - 127)[:, None]).reshape(-1)
