@@ -119,6 +119,7 @@ bool workspace_layout(const Shapes &s, Workspace *ws)
     bytes[MOE_WS_XS_TILES] = xs_tiles;       stride[MOE_WS_XS_TILES] = stage_groups(s.d) * kBlockScaleBytes;
     bytes[MOE_WS_PLAN_COUNTS] = plan_scratch_bytes((long long)P, s.E);
     stride[MOE_WS_PLAN_COUNTS] = (size_t)s.E * 4;
+    bytes[MOE_WS_TILE_DONE] = (tiles + 1) * 4; stride[MOE_WS_TILE_DONE] = 4;
     size_t off = 0;
     for (int i = 0; i < MOE_WS_COUNT; i++) {
         ws->off[i] = off;
@@ -301,7 +302,8 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     if (e == cudaSuccess)
         e = launch_plan(topk_idx, offs, sorted_pair, pair_pos, tile_prefix,
                         reinterpret_cast<int *>(at(MOE_WS_PLAN_COUNTS)), T, E, k, di->status, s, xs, xs_stride,
-                        xs_tiles, d, gemm_tile_rows(P, E));
+                        xs_tiles, d, gemm_tile_rows(P, E), reinterpret_cast<int *>(at(MOE_WS_TILE_DONE)),
+                        (int)max_row_tiles(P, E, gemm_tile_rows(P, E)) + 1);
     // Dense tiles (more than 64 pairs) read A as one box of an expert-ordered
     // copy; below 16 pairs per expert on average dense tiles are rare and the
     // copy is skipped (every tile then gathers).  Either way the rows the MMA
@@ -322,6 +324,8 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     g.timeout_ns = timeout_ns();
     g.num_sms = di->num_sms;
     g.tile_rows = gemm_tile_rows(P, E);
+    g.tile_done = reinterpret_cast<int *>(at(MOE_WS_TILE_DONE));
+    g.all_done = g.tile_done + max_row_tiles(P, E, g.tile_rows);
     if (e == cudaSuccess) {
         g.a = xq;
         g.a_dense = xq_sorted;

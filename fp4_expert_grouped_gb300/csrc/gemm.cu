@@ -178,9 +178,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_alloc(tmem_holder, TMEM_COLS);
         tmem_relinquish();
     }
-    // everything above overlaps the previous kernel's tail; the plan and the
-    // A operand are its outputs
-    pdl_wait();
+    // Everything above overlaps the previous kernel's tail.  GEMM1 waits for
+    // its inputs (the plan, the dispatch copy).  GEMM2 does not wait for GEMM1
+    // to finish: the plan it reads was complete before GEMM1 started, and each
+    // of its row tiles waits for that tile's GEMM1 epilogue warps (tile_done)
+    // before loading the tile's hq rows, so GEMM2 tiles of early experts run
+    // while GEMM1 finishes the last ones.
+    if (MODE == 1) pdl_wait();
     for (int i = threadIdx.x; i <= E; i += NUM_THREADS) {
         s_offs[i] = g.expert_offsets[i];
         s_tp[i] = g.tile_prefix[i];
@@ -188,6 +192,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // GEMM1: let GEMM2 launch now; its CTAs take each SM a GEMM1 CTA leaves
+    if (MODE == 1) pdl_trigger();
     const uint32_t tmem = *tmem_holder;
 
     const int nb = (MODE == 1) ? out_dim / 128 : out_dim / BN;
@@ -210,6 +216,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t stage = 0, phase = 0;
         const int nkt = g.K / 128;                         // K blocks per weight row block
         const int ga = stage_groups(g.K);                   // activation scale groups per tile
+        bool gemm1_done = false;                            // GEMM2: all of GEMM1's tiles published
         for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
             const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb, TR);
             int rb0, rb1;
@@ -232,6 +239,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                               : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
             const uint32_t stage_tx = a_tx + B_STAGE_TX + SFA_STAGE + SFB_STAGE;
             const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
+            // GEMM2: the tile's hq rows and scales are complete once every GEMM1
+            // epilogue warp that stores them (one per 128-channel block of
+            // inter and per working epilogue warp) has published its part
+            // (once GEMM1 has finished altogether no tile needs to wait: the
+            // first look at the total usually says so, costing one load per CTA)
+            if (MODE == 2 && !gemm1_done) {
+                const int per_tile = (TR == 16 ? 2 : EPI_WARPS) * (g.K / 128);
+                if (lane == 0) {
+                    if (ld_acquire(g.all_done) >= per_tile * s_tp[E]) {
+                        gemm1_done = true;
+                        fence_proxy_async_global();
+                    } else if (wait_counter(g.tile_done + ti.m_tile, per_tile, tmo, abort_flag)) {
+                        fence_proxy_async_global();
+                    } else {
+                        *abort_flag = 1;
+                    }
+                }
+                gemm1_done = __shfl_sync(0xffffffffu, gemm1_done, 0);
+                if (*abort_flag) break;
+            }
             // GEMM1: lane l gathers rows 4l .. 4l+3 of the tile, i.e. the xq
             // rows of their tokens; rows past the tile's last valid row repeat
             // its token, so every gathered row is in bounds
@@ -408,6 +435,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         g.hs_tiles[((size_t)ti.m_tile * stage_groups(out_dim) + (ti.n_block >> 2)) * SFA_STAGE +
                                    sf_byte(r, ti.n_block & 3)] = (uint8_t)(e + 127);
                 }
+                // this warp's rows of the tile are stored: publish them to GEMM2
+                __syncwarp();
+                if (lane == 0) {
+                    red_release_add(g.tile_done + ti.m_tile, 1);
+                    red_release_add(g.all_done, 1);
+                }
             } else {
                 uint32_t v0[32], v1[32], v2[32], v3[32];
                 tmem_ld32(trow + 128 * half, v0);
@@ -438,7 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
-    pdl_trigger();
+    if (MODE == 2) pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

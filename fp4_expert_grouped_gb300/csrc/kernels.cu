@@ -510,9 +510,12 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
                                                                        int E, unsigned *status,
                                                                        const uint8_t *__restrict__ xs, int xs_stride,
                                                                        uint8_t *__restrict__ xs_tiles, int G4, int k,
-                                                                       int tile_rows)
+                                                                       int tile_rows, int *__restrict__ tile_done,
+                                                                       int n_tile_done)
 {
     pdl_wait();
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_tile_done; i += blockDim.x) tile_done[i] = 0;
     extern __shared__ int cnt[];                  // [kPlanWarps][E]
     __shared__ int tot[257];                      // per-expert total, then this CTA's first slot
     __shared__ int pre[257];                      // pairs of the expert in earlier CTAs
@@ -630,7 +633,8 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
 
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
                         int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st,
-                        const uint8_t *xs, int xs_stride, uint8_t *xs_tiles, int d, int tile_rows)
+                        const uint8_t *xs, int xs_stride, uint8_t *xs_tiles, int d, int tile_rows, int *tile_done,
+                        int n_tile_done)
 {
     const int G4 = xs_tiles ? stage_groups(d) : 0;
     const long long P = (long long)T * k;
@@ -639,14 +643,14 @@ cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_
     if (C <= 1 || !cta_counts) {
         return launch_pdl(plan_scatter_kernel, dim3(1), dim3(kPlanWarps * 32), smem, st, topk_idx, (const int *)nullptr,
                           expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs, xs_stride, xs_tiles, G4,
-                          k, tile_rows);
+                          k, tile_rows, tile_done, n_tile_done);
     }
     cudaError_t err = launch_pdl(plan_count_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                                  cta_counts, P, E, status);
     if (err != cudaSuccess) return err;
     return launch_pdl(plan_scatter_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                       (const int *)cta_counts, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs,
-                      xs_stride, xs_tiles, G4, k, tile_rows);
+                      xs_stride, xs_tiles, G4, k, tile_rows, tile_done, n_tile_done);
 }
 
 // Scratch for the multi-CTA plan: per-CTA expert counts.

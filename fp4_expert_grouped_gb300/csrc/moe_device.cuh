@@ -106,6 +106,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
 }
 
 // ---------------------------------------------------------------------------
+// Cross-CTA release/acquire counters (GPU scope)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void red_release_add(int *p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded) until *p >= target; false on a timeout or once *abort is set.
+__device__ __forceinline__ bool wait_counter(const int *p, int target, uint64_t timeout_ns, const volatile int *abort)
+{
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire(p) >= target) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// Order this thread's earlier generic-proxy observations of global memory
+// before its later asynchronous-proxy (TMA / bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Asynchronous copies
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)

@@ -108,7 +108,7 @@ cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const 
 cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_t *sorted_pair, int32_t *pair_pos,
                         int32_t *tile_prefix, int *cta_counts, int T, int E, int k, unsigned *status, cudaStream_t st,
                         const uint8_t *xs = nullptr, int xs_stride = 0, uint8_t *xs_tiles = nullptr, int d = 0,
-                        int tile_rows = kTileM);
+                        int tile_rows = kTileM, int *tile_done = nullptr, int n_tile_done = 0);
 size_t plan_scratch_bytes(long long P, int E);
 // Tiles holding more than kDenseTileRows pairs read their A rows as one TMA
 // box from an expert-ordered copy (written by launch_dispatch_dense); the
@@ -129,6 +129,10 @@ struct GemmArgs {
     // expert order.  Scales per 128-row tile in the 512-byte order,
     // [tiles][stage_groups(K)][512].
     int tile_rows;                   // gemm_tile_rows(P, E): 16 or 128 pair rows per tile
+    // per row tile: GEMM1 epilogue warps done with its hq rows and scales
+    // (GEMM1 adds, GEMM2 waits for all of them; zeroed by the plan)
+    int *tile_done;
+    int *all_done;                   // the same arrivals summed over all row tiles
     const uint8_t *a;
     // GEMM1 only: expert-ordered copy of the A rows of the tiles holding more
     // than kDenseTileRows pairs ([P][K]; NULL: every tile gathers)

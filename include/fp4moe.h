@@ -244,6 +244,9 @@ enum {
     MOE_WS_XS_TILES,      /* scales of the expert-ordered pair rows (their tokens' xs), laid
                              out like MOE_WS_HS_TILES with d */
     MOE_WS_PLAN_COUNTS,   /* int32 per-chunk expert counts of the dispatch plan (large batches) */
+    MOE_WS_TILE_DONE,     /* int32 per GEMM row tile: GEMM1 epilogue warps that have stored
+                             the tile's hq rows and scales (GEMM2 starts a row tile once all
+                             of them have), then one int32 total over all tiles */
     MOE_WS_COUNT
 };
 size_t moe_workspace_layout(int T, int d, int inter, int E, int k,

@@ -109,7 +109,7 @@ def test_workspace_layout(capi):
         chunks = (P + 2047) // 2048
         sizes = [T * d, T * xs, T * E * 4, P * 4, P * 4, (E + 1) * 4, P * 4, P * 4, (E + 1) * 4,
                  P * inter, tiles * gh * 512, P * d * 2, P * d, tiles * gx * 512,
-                 chunks * E * 4 if chunks > 1 else 0]
+                 chunks * E * 4 if chunks > 1 else 0, (tiles + 1) * 4]
         assert len(sizes) == capi.MOE_WS_COUNT
         for i in range(capi.MOE_WS_COUNT):
             assert off[i] % 256 == 0
