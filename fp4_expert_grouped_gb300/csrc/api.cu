@@ -304,9 +304,10 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
                         reinterpret_cast<int *>(at(MOE_WS_PLAN_COUNTS)), T, E, k, di->status, s, xs, xs_stride,
                         xs_tiles, d, gemm_tile_rows(P, E), reinterpret_cast<int *>(at(MOE_WS_TILE_DONE)),
                         (int)max_row_tiles(P, E, gemm_tile_rows(P, E)) + 1);
-    // Dense tiles (more than 64 pairs) read A as one box of an expert-ordered
-    // copy; below 16 pairs per expert on average dense tiles are rare and the
-    // copy is skipped (every tile then gathers).  Either way the rows the MMA
+    // From 16 pairs per expert on average, tiles of more than 16 pairs read A
+    // from an expert-ordered copy.  Smaller batches gather every tile and skip
+    // the copy: their GEMM1 streams weights, and the gather-only kernel (a
+    // smaller producer loop) does that faster.  Either way the rows the MMA
     // sees for valid pairs are the same bytes, so the output does not depend
     // on this choice.
     mark(MOE_STAGE_DISPATCH);

@@ -133,6 +133,7 @@ __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, con
 template <int MODE, bool DENSE, int TR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                        const __grid_constant__ CUtensorMap tmA3,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g, const int out_dim)
 {
     using C = Cfg<TR>;
@@ -172,6 +173,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmA2);
+        if (DENSE) tma_prefetch_desc(&tmA3);
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
@@ -231,11 +233,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const long long blk1 = ((long long)ti.e * (g.N / 128) + rb1 / 128) * nkt;
             const bool small = TR == 16 || ti.valid <= SMALL_TILE_ROWS;   // 16-row tiles: always 16-row boxes
             const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
-            // GEMM1: a dense tile reads its rows as one box of the expert-ordered
-            // copy, a sparse one gathers them (four rows per TMA gather)
+            // GEMM1: a dense tile reads its rows from the expert-ordered copy, a
+            // sparse one gathers them (four rows per TMA gather)
             const bool dense = DENSE && ti.valid > kDenseTileRows;
+            // a dense tile of at most 32 rows loads one 32-row box of the copy,
+            // a larger one one 128-row box: one TMA request either way (the
+            // requests, not the bytes, are what an A stage costs)
+            const bool dense_small = dense && ti.valid <= kDenseBoxRows;
             const int a_gathers = (MODE == 1 && !dense) ? (ti.valid + 3) / 4 : 0;
-            const uint32_t a_tx = (MODE == 1) ? (dense ? (uint32_t)A_STAGE : (uint32_t)a_gathers * 4 * BK)
+            const uint32_t a_tx = (MODE == 1) ? (dense ? (dense_small ? (uint32_t)kDenseBoxRows * BK : (uint32_t)A_STAGE)
+                                                       : (uint32_t)a_gathers * 4 * BK)
                                               : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
             const uint32_t stage_tx = a_tx + B_STAGE_TX + SFA_STAGE + SFB_STAGE;
             const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
@@ -280,7 +287,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint64_t *fb = &full[stage];
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, stage_tx);
-                    if (dense) tma_load_2d(sa, &tmA2, fb, ks * BK, ti.row0);
+                    if (dense) tma_load_2d(sa, dense_small ? &tmA3 : &tmA2, fb, ks * BK, ti.row0);
                     if (MODE == 2) {
                         if (small) {
                             for (int b = 0; b < a_boxes; b++)
@@ -537,13 +544,15 @@ template <int MODE>
 static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
 {
     if (a.P == 0) return cudaSuccess;
-    CUtensorMap ma, ma2, mb;
+    CUtensorMap ma, ma2, ma3, mb;
     // GEMM1 gathers single rows of xq (box one row high); GEMM2 reads
     // contiguous expert-ordered rows of hq.  The second A map: GEMM1 -- 128-row
     // boxes of the dense tiles' copy (when there is one); GEMM2 -- 16-row boxes.
+    // The third: GEMM1 -- 32-row boxes of the copy.
     if (!make_map_a(&ma, a.a, a.a_rows, a.K, MODE == 1 ? 1 : gg::BM)) return cudaErrorInvalidValue;
     if (MODE == 1 && a.a_dense) {
         if (!make_map_a(&ma2, a.a_dense, a.P, a.K, gg::BM)) return cudaErrorInvalidValue;
+        if (!make_map_a(&ma3, a.a_dense, a.P, a.K, kDenseBoxRows)) return cudaErrorInvalidValue;
     } else if (!make_map_a(&ma2, a.a, a.a_rows, a.K, MODE == 1 ? 1 : gg::A_SMALL_ROWS)) {
         return cudaErrorInvalidValue;
     }
@@ -567,7 +576,8 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     const int nb = (MODE == 1) ? out_dim / 128 : out_dim / gg::BN;
     const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
-    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), smem, st, ma, ma2, mb, a, out_dim);
+    if (!(MODE == 1 && a.a_dense)) ma3 = ma2;   // unused
+    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), smem, st, ma, ma2, ma3, mb, a, out_dim);
 }
 
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm<1>(a, inter, st); }

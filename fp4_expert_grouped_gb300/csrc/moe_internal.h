@@ -110,10 +110,14 @@ cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_
                         const uint8_t *xs = nullptr, int xs_stride = 0, uint8_t *xs_tiles = nullptr, int d = 0,
                         int tile_rows = kTileM, int *tile_done = nullptr, int n_tile_done = 0);
 size_t plan_scratch_bytes(long long P, int E);
-// Tiles holding more than kDenseTileRows pairs read their A rows as one TMA
-// box from an expert-ordered copy (written by launch_dispatch_dense); the
-// others gather them from xq row by row inside GEMM1.
-constexpr int kDenseTileRows = 64;
+// With 128-row tiles, tiles holding more than kDenseTileRows pairs read their
+// A rows from an expert-ordered copy (written by launch_dispatch_dense): one
+// TMA box of kDenseBoxRows rows when they fit, else one 128-row box; the
+// others gather them from xq, four rows per TMA gather, inside GEMM1.  An A
+// stage costs about one TMA request's worth per box or gather whatever its
+// bytes: four-row gathers suit a handful of rows, a single box the rest.
+constexpr int kDenseTileRows = 16;
+constexpr int kDenseBoxRows = 32;
 // copy of xq row sorted_pair[pos] / k into row pos of xq_sorted, for every pos
 // of a tile holding more than kDenseTileRows pairs
 cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *sorted_pair, const int32_t *topk_idx,

@@ -239,8 +239,9 @@ enum {
                              and group 4g + j at (r % 32) * 16 + (r / 32) * 4 + j */
     MOE_WS_Y,             /* bf16 [P][d], rows in expert order */
     MOE_WS_XQ_SORTED,     /* uint8 E4M3 [P][d]: row p = xq of the pair's token, expert order;
-                             written only for the rows of tiles holding more than 64 pairs
-                             (the others are gathered from xq inside GEMM1) */
+                             written only when T*k >= 16*E, for the rows of tiles holding
+                             more than 16 pairs (the others are gathered from xq inside
+                             GEMM1) */
     MOE_WS_XS_TILES,      /* scales of the expert-ordered pair rows (their tokens' xs), laid
                              out like MOE_WS_HS_TILES with d */
     MOE_WS_PLAN_COUNTS,   /* int32 per-chunk expert counts of the dispatch plan (large batches) */

@@ -363,8 +363,9 @@ def test_workspace_intermediates_tiny():
 
 
 def test_dense_copy_and_gathered_tiles_agree():
-    """Tiles of more than 64 pairs read their A rows from the expert-ordered
-    copy, the others gather them from xq inside GEMM1, and a batch of under 16
+    """With 128-row tiles, tiles of more than 16 pairs read their A rows from
+    the expert-ordered copy (one 32-row box up to 32 rows, one 128-row box above),
+    the others gather them from xq inside GEMM1, and a batch of under 16
     pairs per expert gathers every tile.  The copied rows are xq bit for bit,
     the layer is within tolerance of the oracle, and a token's output is the
     same bits whichever way its tile was loaded."""
@@ -387,7 +388,7 @@ def test_dense_copy_and_gathered_tiles_agree():
         n = int(offs[e + 1] - offs[e])
         for t0 in range(0, n, 128):
             rows = min(128, n - t0)
-            if rows <= 64:
+            if rows <= 16:
                 sparse += 1
                 continue
             dense += 1
