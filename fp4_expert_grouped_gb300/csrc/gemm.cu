@@ -244,7 +244,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t a_tx = (MODE == 1) ? (dense ? (dense_small ? (uint32_t)kDenseBoxRows * BK : (uint32_t)A_STAGE)
                                                        : (uint32_t)a_gathers * 4 * BK)
                                               : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
-            const uint32_t stage_tx = a_tx + B_STAGE_TX + SFA_STAGE + SFB_STAGE;
+            // A's scales change every fourth stage, and only those stages' copy is
+            // read (the MMA thread moves it into tensor memory there)
+            const uint32_t stage_tx = a_tx + B_STAGE_TX + SFB_STAGE;
             const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
             // GEMM2: the tile's hq rows and scales are complete once every GEMM1
             // epilogue warp that stores them (one per 128-channel block of
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint8_t *sb = smem + OFF_B + stage * B_STAGE;
                 uint64_t *fb = &full[stage];
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, stage_tx);
+                    mbar_arrive_expect_tx(fb, stage_tx + ((ks & 3) == 0 ? SFA_STAGE : 0));
                     if (dense) tma_load_2d(sa, dense_small ? &tmA3 : &tmA2, fb, ks * BK, ti.row0);
                     if (MODE == 2) {
                         if (small) {
@@ -298,7 +300,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk0 + ks));
                     tma_load_3d(sb + B_HALF, &tmB, fb, 0, 0, (int)(blk1 + ks));
-                    bulk_copy_g2s(smem + OFF_SFA + stage * SFA_STAGE, a_sf + (ks >> 2) * SFA_STAGE, SFA_STAGE, fb);
+                    if ((ks & 3) == 0)
+                        bulk_copy_g2s(smem + OFF_SFA + stage * SFA_STAGE, a_sf + (ks >> 2) * SFA_STAGE, SFA_STAGE, fb);
                     uint8_t *sfb = smem + OFF_SFB + stage * SFB_STAGE;
                     bulk_copy_g2s(sfb, g.b_scale + (blk0 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
                     bulk_copy_g2s(sfb + 512, g.b_scale + (blk1 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
