@@ -158,7 +158,7 @@ moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E,
     if (!w || !w_fp4 || !w_scale) return MOE_ERR_INVALID_ARG;
     if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
     if (!aligned(w, 16) || !aligned(w_fp4, 16) || !aligned(w_scale, 16)) return MOE_ERR_INVALID_ARG;
-    if (K % 128 || N % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (K % 128 || N % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((long long)E * N * K == 0) return MOE_OK;
     DeviceInfo *di;
     moe_status st = device_info(&di);

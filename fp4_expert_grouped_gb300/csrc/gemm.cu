@@ -48,7 +48,6 @@ constexpr int SMALL_TILE_ROWS = 64;
 constexpr int SFA_STAGE = 512;            // 128 rows x 4 bytes
 constexpr int SFB_STAGE = 1024;           // 256 rows x 4 bytes
 constexpr int B_STAGE = BN * BK;          // 32 KB: 256 rows x 128 codes, one byte per code in shared memory
-constexpr int B_HALF = B_STAGE / 2;
 constexpr int PLAN_INTS = 260;
 constexpr int EPI_WARPS = 8;              // two warps per 32-lane quarter of tensor memory
 constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
@@ -216,21 +215,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // (Prefetching B into L2 ahead of the ring was measured and made every
         // workload slower.)
         uint32_t stage = 0, phase = 0;
-        const int nkt = g.K / 128;                         // K blocks per weight row block
         const int ga = stage_groups(g.K);                   // activation scale groups per tile
         bool gemm1_done = false;                            // GEMM2: all of GEMM1's tiles published
         for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
             const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb, TR);
-            int rb0, rb1;
-            if (MODE == 1) {
-                rb0 = ti.n_block * 128;
-                rb1 = out_dim + ti.n_block * 128;
-            } else {
-                rb0 = ti.n_block * BN;
-                rb1 = rb0 + 128;
-            }
-            const long long blk0 = ((long long)ti.e * (g.N / 128) + rb0 / 128) * nkt;
-            const long long blk1 = ((long long)ti.e * (g.N / 128) + rb1 / 128) * nkt;
+            // The tile's two 128-row weight blocks (GEMM1: gate rows and up rows
+            // of channels [128 t, 128 t + 128); GEMM2: output rows [128 t, +128)
+            // and [d/2 + 128 t, +128)) are adjacent blocks of the tiled layout,
+            // pair t: blocks blk + 2 ks and blk + 2 ks + 1.
+            const long long blk = weight_block(ti.e, ti.n_block, 0, g.N, g.K);
             const bool small = TR == 16 || ti.valid <= SMALL_TILE_ROWS;   // 16-row tiles: always 16-row boxes
             const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
             // GEMM1: a dense tile reads its rows from the expert-ordered copy, a
@@ -298,13 +291,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tma_load_2d(sa, &tmA, fb, ks * BK, ti.row0);
                         }
                     }
-                    tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk0 + ks));
-                    tma_load_3d(sb + B_HALF, &tmB, fb, 0, 0, (int)(blk1 + ks));
+                    tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk + 2 * ks));
                     if ((ks & 3) == 0)
                         bulk_copy_g2s(smem + OFF_SFA + stage * SFA_STAGE, a_sf + (ks >> 2) * SFA_STAGE, SFA_STAGE, fb);
                     uint8_t *sfb = smem + OFF_SFB + stage * SFB_STAGE;
-                    bulk_copy_g2s(sfb, g.b_scale + (blk0 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
-                    bulk_copy_g2s(sfb + 512, g.b_scale + (blk1 + ks) * kBlockScaleBytes, kBlockScaleBytes, fb);
+                    bulk_copy_g2s(sfb, g.b_scale + (blk + 2 * ks) * kBlockScaleBytes, 2 * kBlockScaleBytes, fb);
                 }
                 if (MODE == 1) {
                     __syncwarp();   // the stage's expect_tx is armed before any gather lands
@@ -461,7 +452,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(acc_empty);
                 if (r < ti.valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(g.y + row * out_dim + (size_t)ti.n_block * BN + 128 * half);
+                    // accumulator half h holds output columns of weight block
+                    // n_block + h * d/256 (the tile's pair of blocks)
+                    uint4 *dst = reinterpret_cast<uint4 *>(g.y + row * out_dim +
+                                                           (size_t)(ti.n_block + half * (out_dim / 256)) * 128);
 #pragma unroll
                     for (int c = 0; c < 4; c++) {
                         const uint32_t *v = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
@@ -528,15 +522,16 @@ static bool make_map_a(CUtensorMap *m, const uint8_t *a, long long rows, int K, 
 
 // B operand: tiled MXFP4 codes, 128 x 128 blocks of 8 KB (row r at r * 64);
 // the copy engine spreads each 8-byte group of 16 codes over 16 bytes of
-// shared memory, the layout the FP8/FP6/FP4 MMA reads.  One block per box,
-// 128-byte swizzle.
+// shared memory, the layout the FP8/FP6/FP4 MMA reads.  Two adjacent blocks
+// (a tile's pair) per box, landing as its two 128-row halves; 128-byte
+// swizzle.
 static bool make_map_b(CUtensorMap *m, const uint8_t *b, long long blocks)
 {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {128, 128, (cuuint64_t)blocks};
     cuuint64_t strides[2] = {64, (cuuint64_t)kBlockCodeBytes};
-    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t box[3] = {128, 128, 2};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t *>(b), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -22,8 +22,8 @@ namespace fp4moe {
 // consecutive K elements; four threads share a 32-element block (scale
 // X = floor(log2 amax) - 2, codes = RNE E2M1 of w * 2^-X saturated to +-6,
 // low nibble = even element).  The codes of row n, columns k..k+7 land at
-// block b = (e * N/128 + n/128) * K/128 + k/128, row n % 128, byte (k % 128)/2;
-// the scale byte at b * 512 + sf_byte(n % 128, (k % 128) / 32).
+// block b = weight_block(e, n/128, k/128), row n % 128, byte (k % 128)/2; the
+// scale byte at b * 512 + sf_byte(n % 128, (k % 128) / 32).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pack_fp4_kernel(const float *__restrict__ w, uint8_t *__restrict__ w_fp4,
                                                        uint8_t *__restrict__ w_scale, long long n8, int N, int K)
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(const float *__restrict__
         const int k0 = (int)(el % K);
         const long long e = row / N;
         const int n = (int)(row % N);
-        const long long blk = (e * (N / 128) + n / 128) * (K / 128) + k0 / 128;
+        const long long blk = weight_block(e, n / 128, k0 / 128, N, K);
         const int r = n % 128;
         *reinterpret_cast<uint32_t *>(w_fp4 + blk * kBlockCodeBytes + r * 64 + (k0 % 128) / 2) = codes;
         if ((gid & 3) == 0) w_scale[blk * kBlockScaleBytes + sf_byte(r, (k0 % 128) / 32)] = (uint8_t)(X + 127);

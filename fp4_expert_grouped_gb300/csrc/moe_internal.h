@@ -21,8 +21,13 @@ constexpr int kTileN = 256;   // weight rows per tile = MMA N
 constexpr int kTileK = 128;   // K per pipeline stage
 
 // Tiled MXFP4 weight layout written by moe_pack_fp4 (see fp4moe.h): the
-// matrix [N][K] of an expert is cut into 128 x 128 blocks, numbered
-// ((e * N/128 + n/128) * K/128 + k/128).  Block b holds
+// matrix [N][K] of an expert is cut into 128 x 128 blocks.  The 128-row block
+// n/128 = h * N/256 + j (half h of N, pair j) at K block k/128 is block
+//   b = ((e * N/256 + j) * K/128 + k/128) * 2 + h,
+// so the two blocks a GEMM tile multiplies in one stage -- a 128-row block and
+// its partner N/2 rows further (W13: the gate rows and the up rows of the same
+// channels) -- are adjacent: one TMA box and one scale copy fetch both.
+// Block b holds
 //   codes:  8192 bytes at b * 8192, row r (0..127) at r * 64, two codes per
 //           byte, low nibble = even k
 //   scales: 512 bytes at b * 512, the UE8M0 byte of row r and 32-element
@@ -30,6 +35,11 @@ constexpr int kTileK = 128;   // K per pipeline stage
 //           order the tensor-core scale-factor copy reads.
 constexpr int kBlockCodeBytes = 128 * 64;
 constexpr int kBlockScaleBytes = 512;
+__host__ __device__ inline long long weight_block(long long e, int n128, int k128, int N, int K)
+{
+    const int J = N / 256;
+    return ((e * J + n128 % J) * (K / 128) + k128) * 2 + n128 / J;
+}
 __host__ __device__ inline int sf_byte(int r, int j) { return (r % 32) * 16 + (r / 32) * 4 + j; }
 
 // Activation scales of the GEMM operands (xq rows for GEMM1, hq rows for
@@ -91,7 +101,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // ---- launchers (kernels.cu) ----------------------------------------------
-// rows = E * N; writes the tiled layout above (N % 128 == 0, K % 128 == 0)
+// rows = E * N; writes the tiled layout above (N % 256 == 0, K % 128 == 0)
 cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E, int N, int K, cudaStream_t st);
 cudaError_t launch_quantize(const uint16_t *x, uint8_t *xq, uint8_t *xs, int xs_stride, int T, int d,
                             cudaStream_t st);

@@ -74,8 +74,11 @@ int moe_version(void);
  *            (X = -127 for an all-zero block), clamped to [-127, 127]; codes
  *            are the round-to-nearest-even E2M1 of w * 2^-X saturated to +-6,
  *            the scale is the UE8M0 byte X + 127.
- *   layout   each expert's [N][K] matrix is cut into 128 x 128 blocks,
- *            numbered b = (e * N/128 + n/128) * K/128 + k/128:
+ *   layout   each expert's [N][K] matrix is cut into 128 x 128 blocks; the
+ *            128-row block n/128 = h * N/256 + j (half h of N, pair j) at K
+ *            block k/128 is block b = ((e * N/256 + j) * K/128 + k/128) * 2 + h,
+ *            so a 128-row block and its partner N/2 rows further (for W13 the
+ *            gate and up rows of the same channels) are adjacent:
  *   w_fp4    device, E*N*K/2 bytes: block b at b * 8192, its row n % 128 at
  *            (n % 128) * 64, two codes per byte, the low nibble holding the
  *            even k (so one block is 8 KB of contiguous memory)
@@ -85,7 +88,7 @@ int moe_version(void);
  *            scale-factor copy reads, so the forward loads it with one copy)
  * For the layer: W13 is [E][2*inter][d] (rows 0..inter-1 = gate projection,
  * inter..2*inter-1 = up projection), W2 is [E][d][inter].
- * Requires N % 128 == 0, K % 128 == 0.  Load-time operation, off the hot path.
+ * Requires N % 256 == 0, K % 128 == 0.  Load-time operation, off the hot path.
  */
 moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale,
                         int E, int N, int K, void *stream);

@@ -86,8 +86,9 @@ def test_other_entry_points_reject_bad_arguments(capi):
     lib = capi.lib()
     assert lib.moe_pack_fp4(None, FAKE, FAKE, 1, 128, 128, None) == 1
     assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 128, 96, None) == 2     # K % 128
-    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 64, 128, None) == 2     # N % 128
-    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 0, 128, 128, None) == 0
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 64, 128, None) == 2     # N % 256
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 384, 128, None) == 2
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 0, 256, 128, None) == 0
     assert lib.moe_quantize_act(FAKE, FAKE, FAKE, 4, 100, None) == 2
     assert lib.moe_quantize_act(FAKE, FAKE, FAKE, 0, 128, None) == 0
     assert lib.moe_route(FAKE, FAKE, None, FAKE, FAKE, 4, 128, 8, 9, None) == 2
