@@ -420,17 +420,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int e = e4m3_scale_exp(amax);
                 const float s = exp2i(-e);
                 if (r < ti.valid) {
-                    uint4 *dst =
-                        reinterpret_cast<uint4 *>(g.hq + row * out_dim + (size_t)ti.n_block * 128 + 64 * half);
+                    uint8_t *dst = g.hq + row * out_dim + (size_t)ti.n_block * 128 + 64 * half;
 #pragma unroll
-                    for (int v = 0; v < 4; v++) {
-                        uint32_t w[4];
+                    for (int v = 0; v < 2; v++) {
+                        uint32_t w[8];
 #pragma unroll
-                        for (int u = 0; u < 4; u++) {
-                            const int b = 16 * v + 4 * u;
+                        for (int u = 0; u < 8; u++) {
+                            const int b = 32 * v + 4 * u;
                             w[u] = cvt_e4m3x2(h[b] * s, h[b + 1] * s) | (cvt_e4m3x2(h[b + 2] * s, h[b + 3] * s) << 16);
                         }
-                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        st_global_v8(dst + 32 * v, w);
                     }
                     if (half == 0)
                         g.hs_tiles[((size_t)ti.m_tile * stage_groups(out_dim) + (ti.n_block >> 2)) * SFA_STAGE +
@@ -454,18 +453,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (r < ti.valid) {
                     // accumulator half h holds output columns of weight block
                     // n_block + h * d/256 (the tile's pair of blocks)
-                    uint4 *dst = reinterpret_cast<uint4 *>(g.y + row * out_dim +
-                                                           (size_t)(ti.n_block + half * (out_dim / 256)) * 128);
+                    uint16_t *dst = g.y + row * out_dim + (size_t)(ti.n_block + half * (out_dim / 256)) * 128;
 #pragma unroll
                     for (int c = 0; c < 4; c++) {
                         const uint32_t *v = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
 #pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            const int b = 8 * j;
-                            dst[4 * c + j] = make_uint4(pack_bf16x2(__uint_as_float(v[b]), __uint_as_float(v[b + 1])),
-                                                        pack_bf16x2(__uint_as_float(v[b + 2]), __uint_as_float(v[b + 3])),
-                                                        pack_bf16x2(__uint_as_float(v[b + 4]), __uint_as_float(v[b + 5])),
-                                                        pack_bf16x2(__uint_as_float(v[b + 6]), __uint_as_float(v[b + 7])));
+                        for (int j = 0; j < 2; j++) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int u = 0; u < 8; u++)
+                                w[u] = pack_bf16x2(__uint_as_float(v[16 * j + 2 * u]), __uint_as_float(v[16 * j + 2 * u + 1]));
+                            st_global_v8(dst + 32 * c + 16 * j, w);
                         }
                     }
                 }
