@@ -313,7 +313,7 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     mark(MOE_STAGE_DISPATCH);
     uint8_t *xq_sorted = P >= 16ll * E ? at(MOE_WS_XQ_SORTED) : nullptr;
     if (e == cudaSuccess && xq_sorted)
-        e = launch_dispatch_dense(xq, sorted_pair, topk_idx, offs, xq_sorted, P, d, k, s);
+        e = launch_dispatch_dense(xq, pair_pos, topk_idx, offs, xq_sorted, T, d, k, s);
     mark(MOE_STAGE_GEMM1);
     GemmArgs g;
     std::memset(&g, 0, sizeof g);

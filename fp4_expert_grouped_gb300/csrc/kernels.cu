@@ -668,80 +668,116 @@ size_t plan_scratch_bytes(long long P, int E)
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ y,
                                                       const int32_t *__restrict__ pair_pos,
                                                       const float *__restrict__ topk_w, uint16_t *__restrict__ out,
-                                                      int T, int d, int k)
+                                                      int T, int d, int k, int out32)
 {
     pdl_wait();
-    const int per_tok = d / 8;
+    // one thread per 16 channels of a token: the k slot rows are loaded up
+    // front (32 bytes each), then added in slot order with fused multiply-adds
+    const int per_tok = d / 16;
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid >= (long long)T * per_tok) return;
-    const int t = (int)(gid / per_tok), c8 = (int)(gid % per_tok);
-    float acc[8];
+    const int t = (int)(gid / per_tok), c16 = (int)(gid % per_tok);
+    uint32_t v[8][8];
+    float w[8];
 #pragma unroll
-    for (int i = 0; i < 8; i++) acc[i] = 0.f;
-    for (int j = 0; j < k; j++) {
-        const float w = __ldg(topk_w + (size_t)t * k + j);
-        const int pos = __ldg(pair_pos + (size_t)t * k + j);
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(y + (size_t)pos * d) + c8);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            acc[2 * i] = fmaf(w, bf16_bits_to_f32(u[i] & 0xFFFFu), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(w, bf16_bits_to_f32(u[i] >> 16), acc[2 * i + 1]);
+    for (int j = 0; j < 8; j++) {
+        if (j < k) {
+            w[j] = __ldg(topk_w + (size_t)t * k + j);
+            const int pos = __ldg(pair_pos + (size_t)t * k + j);
+            ld_global_nc_v8(v[j], y + (size_t)pos * d + 16 * c16);
         }
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4 *>(out + (size_t)t * d)[c8] = o;
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) acc[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        if (j < k) {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                acc[2 * i] = fmaf(w[j], bf16_bits_to_f32(v[j][i] & 0xFFFFu), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(w[j], bf16_bits_to_f32(v[j][i] >> 16), acc[2 * i + 1]);
+            }
+        }
+    }
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) o[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    uint16_t *dst = out + (size_t)t * d + 16 * c16;
+    if (out32) {
+        st_global_v8(dst, o);
+    } else {                                   // out is only 16-byte aligned
+        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
     pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
 // Dense dispatch copy: row pos of the expert-ordered activations is the
 // quantised row of token sorted_pair[pos] / k, written only where pos falls in
-// a tile of more than kDenseTileRows pairs (one warp per row, 16-byte vectors).
+// a tile of more than kDenseTileRows pairs.  One warp per token: its xq row is
+// read once (32-byte vectors) and written to each of its pairs' positions that
+// need it -- reading the row once per pair instead, in expert order, doubled
+// the DRAM traffic (the scattered re-reads of xq do not stay in L2).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) dispatch_dense_kernel(const uint8_t *__restrict__ xq,
-                                                             const int32_t *__restrict__ sorted_pair,
+                                                             const int32_t *__restrict__ pair_pos,
                                                              const int32_t *__restrict__ topk_idx,
                                                              const int32_t *__restrict__ expert_offsets,
-                                                             uint8_t *__restrict__ xq_sorted, long long P, int d, int k)
+                                                             uint8_t *__restrict__ xq_sorted, int T, int d, int k)
 {
     pdl_wait();
-    const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (pos < P) {
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t < T) {
         const int lane = threadIdx.x & 31;
-        const int p = __ldg(sorted_pair + pos);
-        const int e = __ldg(topk_idx + p);
-        const long long begin = __ldg(expert_offsets + e), count = __ldg(expert_offsets + e + 1) - begin;
-        const long long tile_first = (pos - begin) / kTileM * kTileM;
-        if (count - tile_first > kDenseTileRows) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)(p / k) * d);
-            uint4 *dst = reinterpret_cast<uint4 *>(xq_sorted + (size_t)pos * d);
-            for (int i = lane; i < d / 16; i += 32) dst[i] = __ldg(src + i);
+        uint8_t *dst[8];                       // NULL: the pair's tile gathers its rows
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            dst[j] = nullptr;
+            if (j < k) {
+                const int pos = __ldg(pair_pos + (size_t)t * k + j);
+                const int e = __ldg(topk_idx + (size_t)t * k + j);
+                const int begin = __ldg(expert_offsets + e), count = __ldg(expert_offsets + e + 1) - begin;
+                const int tile_first = (pos - begin) / kTileM * kTileM;
+                if (count - tile_first > kDenseTileRows) {
+                    dst[j] = xq_sorted + (size_t)pos * d;
+                    any = true;
+                }
+            }
+        }
+        if (any) {
+            const uint8_t *src = xq + (size_t)t * d;
+            for (int i = lane; i < d / 32; i += 32) {
+                uint32_t r[8];
+                ld_global_nc_v8(r, src + 32 * i);
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (dst[j]) st_global_v8(dst[j] + 32 * i, r);
+            }
         }
     }
     pdl_trigger();
 }
 
-cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *sorted_pair, const int32_t *topk_idx,
-                                  const int32_t *expert_offsets, uint8_t *xq_sorted, long long P, int d, int k,
+cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *pair_pos, const int32_t *topk_idx,
+                                  const int32_t *expert_offsets, uint8_t *xq_sorted, int T, int d, int k,
                                   cudaStream_t st)
 {
-    if (P == 0) return cudaSuccess;
-    return launch_pdl(dispatch_dense_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, st, xq, sorted_pair,
-                      topk_idx, expert_offsets, xq_sorted, P, d, k);
+    if (T == 0) return cudaSuccess;
+    return launch_pdl(dispatch_dense_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, st, xq, pair_pos, topk_idx,
+                      expert_offsets, xq_sorted, T, d, k);
 }
 
 cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,
                            int d, int k, cudaStream_t st)
 {
-    const long long n = (long long)T * (d / 8);
+    const long long n = (long long)T * (d / 16);
     if (n == 0) return cudaSuccess;
+    const int out32 = (reinterpret_cast<uintptr_t>(out) % 32) == 0;
     return launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, y, pair_pos, topk_w, out, T,
-                      d, k);
+                      d, k, out32);
 }
 
 } // namespace fp4moe

@@ -114,6 +114,14 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8])
                  : "memory");
 }
 
+// 32-byte read-only global load (address 32-byte aligned).
+__device__ __forceinline__ void ld_global_nc_v8(uint32_t (&w)[8], const void *p)
+{
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
 // ---------------------------------------------------------------------------
 // Cross-CTA release/acquire counters (GPU scope)
 // ---------------------------------------------------------------------------

@@ -128,10 +128,10 @@ size_t plan_scratch_bytes(long long P, int E);
 // bytes: four-row gathers suit a handful of rows, a single box the rest.
 constexpr int kDenseTileRows = 16;
 constexpr int kDenseBoxRows = 32;
-// copy of xq row sorted_pair[pos] / k into row pos of xq_sorted, for every pos
-// of a tile holding more than kDenseTileRows pairs
-cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *sorted_pair, const int32_t *topk_idx,
-                                  const int32_t *expert_offsets, uint8_t *xq_sorted, long long P, int d, int k,
+// copy of xq row t into row pair_pos[t * k + j] of xq_sorted, for every pair
+// whose position falls in a tile holding more than kDenseTileRows pairs
+cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *pair_pos, const int32_t *topk_idx,
+                                  const int32_t *expert_offsets, uint8_t *xq_sorted, int T, int d, int k,
                                   cudaStream_t st);
 cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,
                            int d, int k, cudaStream_t st);
