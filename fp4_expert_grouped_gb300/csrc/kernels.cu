@@ -95,14 +95,42 @@ __device__ __forceinline__ int quant_group_warp(const uint16_t *__restrict__ xg,
     return e;
 }
 
+// A whole row by one warp: 8 channels per lane, so a step covers two groups
+// (lanes 0-15 the first, each half reducing its own amax); the next step's
+// 16-byte loads are issued before the current step is converted.
 __device__ __forceinline__ void quant_row_warp(const uint16_t *__restrict__ xrow, uint8_t *__restrict__ qrow,
                                                uint8_t *__restrict__ srow, int d, int s_stride)
 {
     const int lane = threadIdx.x & 31;
     const int G = d / 128;
-    for (int g = 0; g < G; g++) {
-        const int e = quant_group_warp(xrow + g * 128, qrow + g * 128);
-        if (lane == 0) srow[g] = (uint8_t)(e + 127);
+    const int n8 = d / 8;                              // 8-channel pieces of the row
+    const uint4 *src = reinterpret_cast<const uint4 *>(xrow);
+    uint4 nxt = make_uint4(0, 0, 0, 0);
+    if (lane < n8) nxt = __ldg(src + lane);
+    for (int c = lane; c - lane < n8; c += 32) {
+        const uint4 cur = nxt;
+        if (c + 32 < n8) nxt = __ldg(src + c + 32);
+        const uint32_t u[4] = {cur.x, cur.y, cur.z, cur.w};
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            v[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
+            v[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (c < n8) {
+            const int e = e4m3_scale_exp(amax);
+            const float sc = exp2i(-e);
+            uint2 q;
+            q.x = cvt_e4m3x2(v[0] * sc, v[1] * sc) | (cvt_e4m3x2(v[2] * sc, v[3] * sc) << 16);
+            q.y = cvt_e4m3x2(v[4] * sc, v[5] * sc) | (cvt_e4m3x2(v[6] * sc, v[7] * sc) << 16);
+            reinterpret_cast<uint2 *>(qrow)[c] = q;
+            if ((lane & 15) == 0) srow[c / 16] = (uint8_t)(e + 127);
+        }
     }
     for (int g = G + lane; g < s_stride; g += 32) srow[g] = 0;
 }
