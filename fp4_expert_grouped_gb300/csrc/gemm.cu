@@ -26,8 +26,11 @@
 //               and 512-byte bulk copies of scale factors stored in the
 //               tensor cores' scale-factor order, into a 4-stage ring
 //   warp 1      tensor-memory owner and MMA issuer (one elected thread):
-//               scale factors -> tensor memory (tcgen05.cp), then 4 MMAs of
-//               K = 32 per stage into a 128 x 256 fp32 accumulator
+//               A's scale factors -> tensor memory (tcgen05.cp, every fourth
+//               stage), then 4 MMAs of K = 32 per stage into a 128 x 256 fp32
+//               accumulator
+//   warp 10     (16-row tiles) B's scale factors -> tensor memory, one copy
+//               pair per stage; otherwise the MMA thread copies them
 //   warps 2-9   epilogue, two warps per 32-lane quarter of tensor memory, each
 //               with half of the columns: tcgen05.ld to registers, release of
 //               the accumulator to the MMA warp, then
@@ -50,7 +53,7 @@ constexpr int SFB_STAGE = 1024;           // 256 rows x 4 bytes
 constexpr int B_STAGE = BN * BK;          // 32 KB: 256 rows x 128 codes, one byte per code in shared memory
 constexpr int PLAN_INTS = 260;
 constexpr int EPI_WARPS = 8;              // two warps per 32-lane quarter of tensor memory
-constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
+constexpr int SF_WARP = 2 + EPI_WARPS;    // B scale-factor copies into tensor memory (16-row tiles)
 
 // Shared-memory layout per tile size TR (pair rows per tile).  TR = 128: a
 // 4-stage ring of 48 KB stages (A 16 KB, B 32 KB).  TR = 16: A slots of 2 KB
@@ -61,6 +64,13 @@ constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
 template <int TR>
 struct Cfg {
     static constexpr int STAGES = TR == 16 ? 6 : 4;
+    // 16-row tiles stream weights through a 6-deep ring: a separate warp copies
+    // B's scale factors into tensor memory, keeping the MMA thread's per-stage
+    // issue work under the stage's MMA time (decode GEMM1 363 -> 352 us).  With
+    // 128-row tiles and a 4-deep ring the extra hop's latency cost more (large
+    // batches 1-3% slower), so there the MMA thread copies them itself.
+    static constexpr bool SF_WARP = TR == 16;
+    static constexpr int NUM_THREADS = (SF_WARP ? 3 + EPI_WARPS : 2 + EPI_WARPS) * 32;
     static constexpr int A_STAGE = TR * BK;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -68,7 +78,8 @@ struct Cfg {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_AMAX = OFF_SFB + STAGES * SFB_STAGE;          // [2 tile parities][2 halves][128 rows] fp32
     static constexpr int OFF_BAR = OFF_AMAX + 2 * 2 * BM * 4;
-    static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2 + 4) * 8;   // + one amax-exchange barrier per lane quarter
+    // full, empty, sf_ready per stage; acc_full, acc_empty; one amax-exchange barrier per lane quarter
+    static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 2 + 4) * 8;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static constexpr int SMEM_USED = OFF_PLAN + 2 * PLAN_INTS * 4;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
@@ -130,12 +141,14 @@ __device__ __forceinline__ Tile decode_tile(long long tile, const int *s_tp, con
 // producer, whose loop is sensitive to its size when the GEMM streams weights.
 // TR: pair rows per tile (16 or 128).
 template <int MODE, bool DENSE, int TR>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmA3,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g, const int out_dim)
 {
     using C = Cfg<TR>;
+    constexpr bool SFW = C::SF_WARP;
+    constexpr int NUM_THREADS = C::NUM_THREADS;
     constexpr int STAGES = C::STAGES;
     constexpr int A_STAGE = C::A_STAGE;
     constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_SFA = C::OFF_SFA, OFF_SFB = C::OFF_SFB;
@@ -144,7 +157,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *empty = full + STAGES;
-    uint64_t *acc_full = full + 2 * STAGES;
+    uint64_t *sf_ready = full + 2 * STAGES;    // the stage's B scale factors are in tensor memory
+    uint64_t *acc_full = full + 3 * STAGES;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *xbar = acc_empty + 1;            // [4] amax exchange of the two epilogue warps of a lane quarter
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
@@ -161,6 +175,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; s++) {
             mbar_init(&full[s], full_arrivals(MODE));
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 1);
         }
         mbar_init(acc_full, 1);
         // 16-row tiles: only the two epilogue warps of lane quarter 0 hold rows
@@ -320,19 +335,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             bool ok = true;
             for (int ks = 0; ks < nk; ks++) {
-                if (!mbar_wait(&full[stage], phase, tmo, abort_flag)) {
+                // the stage's operands have landed and its B scale factors are in
+                // tensor memory (the scale-factor warp waited for the former)
+                if (!mbar_wait(SFW ? &sf_ready[stage] : &full[stage], phase, tmo, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t sfa = sbase + OFF_SFA + stage * SFA_STAGE;
-                    const uint32_t sfb = sbase + OFF_SFB + stage * SFB_STAGE;
                     const uint32_t sfa_col = tmem + SFA_COL0 + ((ks >> 2) & 1) * 4;
                     const uint32_t sfb_col = tmem + SFB_COL0 + stage * SFB_COLS_PER_STAGE;
+                    // A's scales change every fourth stage; copying them here, in
+                    // order with this thread's MMAs, keeps the two slots safe
                     if ((ks & 3) == 0) tc_cp_32x128b_warpx4(sfa_col, sdesc_sf(sfa));
-                    tc_cp_32x128b_warpx4(sfb_col, sdesc_sf(sfb));
-                    tc_cp_32x128b_warpx4(sfb_col + 4, sdesc_sf(sfb + 512));
+                    if (!SFW) {
+                        const uint32_t sfb = sbase + OFF_SFB + stage * SFB_STAGE;
+                        tc_cp_32x128b_warpx4(sfb_col, sdesc_sf(sfb));
+                        tc_cp_32x128b_warpx4(sfb_col + 4, sdesc_sf(sfb + 512));
+                    }
                     const uint64_t adesc = sdesc_kmajor_sw128(sbase + OFF_A + stage * A_STAGE);
                     const uint64_t bdesc = sdesc_kmajor_sw128(sbase + OFF_B + stage * B_STAGE);
 #pragma unroll
@@ -359,6 +380,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             acc_phase ^= 1u;
         }
+    } else if (SFW && warp == SF_WARP) {
+        // ------------------------------------------------------- B scale factors
+        // Same tile and stage walk as the MMA warp: once a stage is full, copy
+        // its B scale factors into the stage's tensor-memory columns and signal
+        // sf_ready.  This keeps the two copies per stage off the MMA thread,
+        // whose per-stage issue work must stay under the stage's MMA time.  The
+        // copies wait for the stage's full barrier, which completes only once
+        // the MMAs of the stage's previous use have finished.
+        uint32_t stage = 0, phase = 0;
+        const uint32_t sbase = smem_u32(smem);
+        bool ok = true;
+        for (long long tile = blockIdx.x; ok && tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+            for (int ks = 0; ks < nk; ks++) {
+                if (!mbar_wait(&full[stage], phase, tmo, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sfb = sbase + OFF_SFB + stage * SFB_STAGE;
+                    const uint32_t sfb_col = tmem + SFB_COL0 + stage * SFB_COLS_PER_STAGE;
+                    tc_cp_32x128b_warpx4(sfb_col, sdesc_sf(sfb));
+                    tc_cp_32x128b_warpx4(sfb_col + 4, sdesc_sf(sfb + 512));
+                    tc_commit(&sf_ready[stage]);
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) *abort_flag = 1;
     } else {
         // ------------------------------------------------------------ epilogue
         // Eight warps: warp w reads tensor-memory lanes 32 * (w % 4) ..; the two
@@ -573,7 +627,8 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
     if (!(MODE == 1 && a.a_dense)) ma3 = ma2;   // unused
-    return launch_pdl(kern, dim3(grid), dim3(gg::NUM_THREADS), smem, st, ma, ma2, ma3, mb, a, out_dim);
+    const int threads = a.tile_rows == 16 ? gg::Cfg<16>::NUM_THREADS : gg::Cfg<128>::NUM_THREADS;
+    return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ma, ma2, ma3, mb, a, out_dim);
 }
 
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm<1>(a, inter, st); }
