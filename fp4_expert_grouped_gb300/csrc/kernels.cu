@@ -13,6 +13,7 @@
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
+#include <algorithm>
 #include <climits>
 
 namespace fp4moe {
@@ -479,9 +480,15 @@ cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const 
 // offsets, gives each warp the first free slot per expert of its chunk, then
 // walks its pairs in order placing each at slot + rank among equal experts
 // earlier in the step.  The result is the unique stable order.
+// Up to kPlanFusedMaxPairs pairs a single kernel does it all: each of its
+// CTAs (kPlanFusedChunk pairs each) counts every pair itself -- the per-expert
+// totals and the pairs before its chunk -- so no CTA waits for another, and
+// the scattered stores of the pairs' scale words spread over many SMs.
 // ---------------------------------------------------------------------------
 constexpr int kPlanWarps = 32;
 constexpr int kPlanPairsPerCta = 2048;
+constexpr int kPlanFusedChunk = 256;
+constexpr long long kPlanFusedMaxPairs = 32768;
 
 // Count this CTA's pairs into the warp rows cnt[warp][e]; returns nothing,
 // flags out-of-range experts (treated as expert 0 so the plan stays a bijection).
@@ -540,7 +547,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
                                                                        const uint8_t *__restrict__ xs, int xs_stride,
                                                                        uint8_t *__restrict__ xs_tiles, int G4, int k,
                                                                        int tile_rows, int *__restrict__ tile_done,
-                                                                       int n_tile_done)
+                                                                       int n_tile_done, int chunk_pairs)
 {
     pdl_wait();
     if (blockIdx.x == 0)
@@ -552,19 +559,58 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
     __shared__ int goff[257];                     // expert's first slot in expert order
     __shared__ int gtp[257];                      // expert's first row tile (tile_rows pairs each)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int C = cta_counts ? gridDim.x : 1;
+    const int C = gridDim.x;
+    // several CTAs and no count kernel: every CTA counts all pairs itself
+    const bool fused = C > 1 && !cta_counts;
     for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        tot[i] = 0;
+        pre[i] = 0;
+    }
     __syncthreads();
-    const long long chunk = cta_counts ? kPlanPairsPerCta : P;
+    const long long chunk = C > 1 ? chunk_pairs : P;
     const long long pb = (long long)blockIdx.x * chunk;
     const long long pe = (pb + chunk < P) ? pb + chunk : P;
     bool bad = false;
     plan_count_warps(topk_idx, cnt, pb, pe, E, &bad);
+    if (fused) {
+        // per-expert totals and pairs before this chunk (order-free counts);
+        // four 16-byte index loads in flight per thread
+        auto count = [&](int e, long long p) {
+            if (e < 0 || e >= E) e = 0;
+            atomicAdd(&tot[e], 1);
+            if (p < pb) atomicAdd(&pre[e], 1);
+        };
+        const long long nv = (reinterpret_cast<uintptr_t>(topk_idx) & 15) ? 0 : P / 4;
+        const int4 *v4 = reinterpret_cast<const int4 *>(topk_idx);
+        for (long long i0 = threadIdx.x; i0 < nv; i0 += 4 * (long long)blockDim.x) {
+            int4 q[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const long long i = i0 + (long long)u * blockDim.x;
+                q[u] = i < nv ? __ldg(v4 + i) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const long long i = i0 + (long long)u * blockDim.x;
+                if (i < nv) {
+                    count(q[u].x, 4 * i);
+                    count(q[u].y, 4 * i + 1);
+                    count(q[u].z, 4 * i + 2);
+                    count(q[u].w, 4 * i + 3);
+                }
+            }
+        }
+        for (long long p = 4 * nv + threadIdx.x; p < P; p += blockDim.x) count(__ldg(topk_idx + p), p);
+    }
     __syncthreads();
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int before = 0, total = 0;
-        if (cta_counts) {
+        if (fused) {
+            before = pre[e];
+            total = tot[e];
+        } else if (cta_counts) {
             for (int c = 0; c < C; c++) {
                 const int v = __ldg(cta_counts + (size_t)c * E + e);
                 if (c < (int)blockIdx.x) before += v;
@@ -650,9 +696,16 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
                 const long long m = gtp[e] + local / tile_rows;
                 const int r = local % tile_rows;
                 const uint32_t *src = reinterpret_cast<const uint32_t *>(xs + (size_t)(p / k) * xs_stride);
-                for (int g = 0; g < G4; g++)
-                    *reinterpret_cast<uint32_t *>(xs_tiles + ((size_t)m * G4 + g) * kBlockScaleBytes + sf_byte(r, 0)) =
-                        __ldg(src + g);
+                uint8_t *dst = xs_tiles + (size_t)m * G4 * kBlockScaleBytes + sf_byte(r, 0);
+                for (int g0 = 0; g0 < G4; g0 += 8) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int u = 0; u < 8; u++) w[u] = g0 + u < G4 ? __ldg(src + g0 + u) : 0u;
+#pragma unroll
+                    for (int u = 0; u < 8; u++)
+                        if (g0 + u < G4)
+                            *reinterpret_cast<uint32_t *>(dst + (size_t)(g0 + u) * kBlockScaleBytes) = w[u];
+                }
             }
         }
     }
@@ -669,17 +722,20 @@ cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_
     const long long P = (long long)T * k;
     const size_t smem = (size_t)kPlanWarps * E * sizeof(int);
     const long long C = (P + kPlanPairsPerCta - 1) / kPlanPairsPerCta;
-    if (C <= 1 || !cta_counts) {
-        return launch_pdl(plan_scatter_kernel, dim3(1), dim3(kPlanWarps * 32), smem, st, topk_idx, (const int *)nullptr,
-                          expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs, xs_stride, xs_tiles, G4,
-                          k, tile_rows, tile_done, n_tile_done);
+    if (P <= kPlanFusedMaxPairs || !cta_counts) {
+        // one kernel: kPlanFusedChunk pairs per CTA up to kPlanFusedMaxPairs
+        // pairs; one CTA for all pairs beyond that when there is no scratch
+        const long long CF = P <= kPlanFusedMaxPairs ? std::max(1LL, (P + kPlanFusedChunk - 1) / kPlanFusedChunk) : 1;
+        return launch_pdl(plan_scatter_kernel, dim3((unsigned)CF), dim3(kPlanWarps * 32), smem, st, topk_idx,
+                          (const int *)nullptr, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs,
+                          xs_stride, xs_tiles, G4, k, tile_rows, tile_done, n_tile_done, kPlanFusedChunk);
     }
     cudaError_t err = launch_pdl(plan_count_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                                  cta_counts, P, E, status);
     if (err != cudaSuccess) return err;
     return launch_pdl(plan_scatter_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                       (const int *)cta_counts, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs,
-                      xs_stride, xs_tiles, G4, k, tile_rows, tile_done, n_tile_done);
+                      xs_stride, xs_tiles, G4, k, tile_rows, tile_done, n_tile_done, kPlanPairsPerCta);
 }
 
 // Scratch for the multi-CTA plan: per-CTA expert counts.

@@ -165,7 +165,8 @@ def test_route_bitexact(T, d, E, k, ties, bias):
 
 
 @pytest.mark.parametrize("T,E,k,skew", [(1, 8, 1, False), (33, 8, 2, False), (128, 256, 8, False),
-                                        (4096, 256, 8, True), (16384, 256, 8, False), (1000, 5, 5, False)])
+                                        (4096, 256, 8, True), (4097, 256, 8, False), (16384, 256, 8, False),
+                                        (1000, 5, 5, False)])
 def test_dispatch_plan_bitexact(T, E, k, skew):
     rng = np.random.default_rng(T + E)
     if skew:
@@ -183,6 +184,26 @@ def test_dispatch_plan_bitexact(T, E, k, skew):
     assert np.array_equal(sp.cpu().numpy(), rs)
     assert np.array_equal(pp.cpu().numpy(), rp)
     assert capi().moe_get_device_status() == 0
+
+
+def test_dispatch_plan_indices_not_16_byte_aligned():
+    """The plan reads the expert indices 16 bytes at a time where their address
+    allows; an index array only 4-byte aligned takes the word-by-word path."""
+    T, E, k = 777, 64, 6
+    rng = np.random.default_rng(5)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    buf = torch.empty(T * k + 1, dtype=torch.int32, device=DEV)
+    buf[1:] = torch.from_numpy(idx.reshape(-1)).to(DEV)
+    view = buf[1:].view(T, k)
+    assert view.data_ptr() % 16 != 0
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    sp = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    pp = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    capi().moe_dispatch_plan(view, offs, sp, pp, E)
+    ro, rs, rp = oracle.dispatch_plan(idx, E)
+    assert np.array_equal(offs.cpu().numpy(), ro)
+    assert np.array_equal(sp.cpu().numpy(), rs)
+    assert np.array_equal(pp.cpu().numpy(), rp)
 
 
 def test_dispatch_plan_flags_bad_expert_index():
