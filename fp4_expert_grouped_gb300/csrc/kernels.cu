@@ -325,21 +325,25 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
                                int E, cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
-    // Tile shapes measured at E = 256 (all give the same bits): a 48 x 32
-    // (token x expert) CTA tile of twelve 8 x 16 warp tiles from 1536 tokens
-    // on, 24 x 16 from 384, 16 x 16 of eight 4 x 8 warp tiles below (T=256:
-    // 43 -> 31 us); 256-channel chunks (fewer block barriers) where d allows.
+    // Tile shapes measured at E = 256 (all give the same bits), as (token x
+    // expert) warp tiles and warps per CTA: 6 x 16 tiles, 4 x 2 warps (two
+    // CTAs of 24 x 32 per SM) from 1536 tokens on (T=2048: 165 -> 135 us,
+    // T=4096: 272 -> 234 us, T=16384 at d=7168: 1489 -> 1457 us against
+    // 8 x 16 tiles of 6 x 2 warps); 4 x 16 tiles, 8 x 1 warps from 192 (T=512:
+    // 60 -> 47 us); 4 x 8 tiles, 4 x 2 warps below.  256-channel chunks
+    // (fewer block barriers) where d allows, else 128 channels.
     // E not a multiple of 4 loads gate_w by words.
     if (E % 4) {
         return T >= 2048 ? launch_gate_cfg<8, 16, 4, 2, false>(x, gate_w, bias, z, T, d, E, st)
                          : launch_gate_cfg<4, 8, 4, 1, false>(x, gate_w, bias, z, T, d, E, st);
     }
     if (d % 256) {
-        return T >= 1536 ? launch_gate_cfg<8, 16, 6, 2, true>(x, gate_w, bias, z, T, d, E, st)
-                         : launch_gate_cfg<4, 8, 4, 1, true>(x, gate_w, bias, z, T, d, E, st);
+        if (T >= 1536) return launch_gate_cfg<6, 16, 4, 2, true, 128, 4>(x, gate_w, bias, z, T, d, E, st);
+        if (T >= 192) return launch_gate_cfg<4, 16, 8, 1, true, 128, 4>(x, gate_w, bias, z, T, d, E, st);
+        return launch_gate_cfg<4, 8, 4, 1, true>(x, gate_w, bias, z, T, d, E, st);
     }
-    if (T >= 1536) return launch_gate_cfg<8, 16, 6, 2, true, 256, 2>(x, gate_w, bias, z, T, d, E, st);
-    if (T >= 384) return launch_gate_cfg<4, 16, 6, 1, true, 256, 3>(x, gate_w, bias, z, T, d, E, st);
+    if (T >= 1536) return launch_gate_cfg<6, 16, 4, 2, true, 256, 2>(x, gate_w, bias, z, T, d, E, st);
+    if (T >= 192) return launch_gate_cfg<4, 16, 8, 1, true, 256, 3>(x, gate_w, bias, z, T, d, E, st);
     return launch_gate_cfg<4, 8, 4, 2, true, 256, 3>(x, gate_w, bias, z, T, d, E, st);
 }
 

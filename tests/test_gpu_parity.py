@@ -145,6 +145,8 @@ def test_quantize_act_bitexact():
     (700, 1280, 64, 6, False, True),      # mid-batch gate tile
     (1600, 640, 32, 4, True, False),      # large batch, d not a multiple of 256 (128-channel chunks)
     (40, 384, 16, 4, False, False),       # small batch, 128-channel chunks
+    (300, 384, 32, 4, False, True),       # mid batch, 128-channel chunks
+    (1540, 256, 40, 4, False, False),     # large batch, E not a multiple of the CTA's 32 experts
 ])
 def test_route_bitexact(T, d, E, k, ties, bias):
     rng = np.random.default_rng(T * 31 + E)
