@@ -180,7 +180,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 } // namespace gate
 
-template <int TW, int EW, int WT, int WE, bool VEC_W, int CH, int STAGES>
+template <int TW, int EW, int WT, int WE, bool VEC_W, int CH, int STAGES, bool PF = false>
 __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t *__restrict__ x,
                                                                   const float *__restrict__ gate_w,
                                                                   const float *__restrict__ bias,
@@ -257,11 +257,9 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
         const int st = c % STAGES;
         const uint16_t *xb = xs_ + st * CT * XROW + (wt * TW) * XROW;
         const float *wb = ws_ + st * CH * WROW + we * EW;
-#pragma unroll
-        for (int q = 0; q < CH / 32; q++) {
-            const int i = q * 32 + lane;         // this lane's channel in the chunk
-            float2 xv[TW];
-            float2 wv[EW / 2];
+        // operands of channel step q (this lane's channel q * 32 + lane)
+        auto load_ops = [&](int q, float2 (&xv)[TW], float2 (&wv)[EW / 2]) {
+            const int i = q * 32 + lane;
 #pragma unroll
             for (int a = 0; a < TW; a++) {
                 const float xf = bf16_bits_to_f32(xb[a * XROW + i]);
@@ -273,10 +271,31 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
                 wv[b / 2] = make_float2(f.x, f.y);
                 wv[b / 2 + 1] = make_float2(f.z, f.w);
             }
+        };
+        if constexpr (PF) {
+            // next step's operands load while this step's multiply-adds issue
+            float2 xv[2][TW];
+            float2 wv[2][EW / 2];
+            load_ops(0, xv[0], wv[0]);
 #pragma unroll
-            for (int a = 0; a < TW; a++)
+            for (int q = 0; q < CH / 32; q++) {
+                if (q + 1 < CH / 32) load_ops(q + 1, xv[(q + 1) & 1], wv[(q + 1) & 1]);
 #pragma unroll
-                for (int b = 0; b < EW / 2; b++) acc[a][b] = __ffma2_rn(xv[a], wv[b], acc[a][b]);
+                for (int a = 0; a < TW; a++)
+#pragma unroll
+                    for (int b = 0; b < EW / 2; b++) acc[a][b] = __ffma2_rn(xv[q & 1][a], wv[q & 1][b], acc[a][b]);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < CH / 32; q++) {
+                float2 xv[TW];
+                float2 wv[EW / 2];
+                load_ops(q, xv, wv);
+#pragma unroll
+                for (int a = 0; a < TW; a++)
+#pragma unroll
+                    for (int b = 0; b < EW / 2; b++) acc[a][b] = __ffma2_rn(xv[a], wv[b], acc[a][b]);
+            }
         }
     }
     cp_async_wait<0>();
@@ -307,17 +326,184 @@ __global__ void __launch_bounds__(WT *WE * 32) gate_logits_kernel(const uint16_t
     pdl_trigger();
 }
 
-template <int TW, int EW, int WT, int WE, bool VEC_W, int CH = 128, int STAGES = 4>
+template <int TW, int EW, int WT, int WE, bool VEC_W, int CH = 128, int STAGES = 4, bool PF = false>
 static cudaError_t launch_gate_cfg(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T, int d,
                                    int E, cudaStream_t st)
 {
     constexpr int CT = TW * WT, CE = EW * WE;
     if (d % CH) return cudaErrorInvalidValue;
     const size_t smem = (size_t)STAGES * (CT * (CH + 8) * 2 + CH * (CE + 4) * 4);
-    auto kern = gate_logits_kernel<TW, EW, WT, WE, VEC_W, CH, STAGES>;
+    auto kern = gate_logits_kernel<TW, EW, WT, WE, VEC_W, CH, STAGES, PF>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid((T + CT - 1) / CT, (E + CE - 1) / CE);
+    return launch_pdl(kern, grid, dim3(WT * WE * 32), smem, st, x, gate_w, bias, z, T, d, E);
+}
+
+// Small batches: the 32 lane partial sums of every logit are split over a
+// cluster of four CTAs, eight each (partial l = 8 g + j in the CTA of cluster
+// rank g), so a batch of a few tiles still spreads over four times as many
+// CTAs, each with a quarter of the channels.  Every partial is the same
+// fused multiply-add chain over its channels in order as in the kernel above.
+// Lane 8 u + j runs partial 8 g + j for tokens [TW u, TW u + TW) of its warp's
+// 4 TW tokens and all EW experts of its warp.  CTA 0 of the cluster then adds
+// the 32 partials of each logit in the same xor-tree order (pairs 16 apart,
+// then 8, 4, 2, 1), reading the other CTAs' partials from their shared memory.
+// Both cluster barriers are taken unconditionally by every thread; the CTAs of
+// a cluster are resident together, so neither can wait forever.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+constexpr int kGateSplit = 4;                 // CTAs per cluster (partial-sum groups)
+
+template <int TW, int EW, int WT, int WE, int CH, int STAGES>
+__global__ void __cluster_dims__(1, 1, kGateSplit) __launch_bounds__(WT *WE * 32)
+    gate_logits_split_kernel(const uint16_t *__restrict__ x, const float *__restrict__ gate_w,
+                             const float *__restrict__ bias, float *__restrict__ z, int T, int d, int E)
+{
+    pdl_wait();
+    using namespace gate;
+    constexpr int L = 32 / kGateSplit;        // partials per CTA
+    constexpr int NT = WT * WE * 32;
+    constexpr int CT = TW * (32 / L) * WT;    // tokens per CTA
+    constexpr int CE = EW * WE;               // experts per CTA
+    constexpr int CC = CH / kGateSplit;       // this CTA's channels of a chunk (L of every 32)
+    constexpr int XROW = CC + 8;              // padded x row (bf16 elements)
+    constexpr int WROW = CE + 4;              // padded gate_w row (floats)
+    static_assert(L == 8, "one 16-byte x copy per 32-channel block");
+    static_assert(CE % 4 == 0 && CH % 32 == 0, "tile shape");
+    static_assert(STAGES * (CT * XROW * 2 + CC * WROW * 4) >= L * CT * CE * 4, "partials fit the staging memory");
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint16_t *xs_ = reinterpret_cast<uint16_t *>(smem_raw);                       // [STAGES][CT][XROW]
+    float *ws_ = reinterpret_cast<float *>(smem_raw + STAGES * CT * XROW * 2);     // [STAGES][CC][WROW]
+    float *part = reinterpret_cast<float *>(smem_raw);                            // [L][CT][CE] after the loop
+
+    const int g = blockIdx.z;                 // rank in the cluster (cluster = the grid's z extent)
+    const int t0 = blockIdx.x * CT;
+    const int e0 = blockIdx.y * CE;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wt = warp / WE, we = warp % WE;
+    const int j = lane % L, u = lane / L;
+    const int nch = d / CH;
+
+    auto load_chunk = [&](int c) {
+        if (c >= nch) return;
+        const int st = c % STAGES;
+        const int i0 = c * CH;
+        uint16_t *xd = xs_ + st * CT * XROW;
+        for (int q = threadIdx.x; q < CT * (CH / 32); q += NT) {
+            const int r = q / (CH / 32), b = q % (CH / 32);
+            const int t = t0 + r;
+            const bool ok = t < T;
+            cp_async_16_zfill(xd + r * XROW + b * L, x + (size_t)(ok ? t : 0) * d + i0 + b * 32 + g * L, ok);
+        }
+        float *wd = ws_ + st * CC * WROW;
+        for (int q = threadIdx.x; q < CC * (CE / 4); q += NT) {
+            const int r = q / (CE / 4), c4 = q % (CE / 4);
+            const int ch = i0 + (r / L) * 32 + g * L + r % L;
+            const int e = e0 + c4 * 4;
+            const bool ok = e < E;
+            cp_async_16_zfill(wd + r * WROW + c4 * 4, gate_w + (size_t)ch * E + (ok ? e : 0), ok);
+        }
+    };
+
+    float2 acc[TW][EW / 2];
+#pragma unroll
+    for (int a = 0; a < TW; a++)
+#pragma unroll
+        for (int b = 0; b < EW / 2; b++) acc[a][b] = make_float2(0.f, 0.f);
+
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; s++) {
+        load_chunk(s);
+        cp_async_commit();
+    }
+    const int tl0 = wt * TW * (32 / L) + u * TW;   // this lane's first token in the CTA tile
+    for (int c = 0; c < nch; c++) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        load_chunk(c + STAGES - 1);
+        cp_async_commit();
+        const int st = c % STAGES;
+        const uint16_t *xb = xs_ + st * CT * XROW + tl0 * XROW;
+        const float *wb = ws_ + st * CC * WROW + we * EW;
+#pragma unroll
+        for (int b = 0; b < CH / 32; b++) {
+            const int i = b * L + j;             // channel 32 b + 8 g + j of the chunk
+            float2 xv[TW];
+            float2 wv[EW / 2];
+#pragma unroll
+            for (int a = 0; a < TW; a++) {
+                const float xf = bf16_bits_to_f32(xb[a * XROW + i]);
+                xv[a] = make_float2(xf, xf);
+            }
+#pragma unroll
+            for (int q = 0; q < EW; q += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(wb + i * WROW + q);
+                wv[q / 2] = make_float2(f.x, f.y);
+                wv[q / 2 + 1] = make_float2(f.z, f.w);
+            }
+#pragma unroll
+            for (int a = 0; a < TW; a++)
+#pragma unroll
+                for (int q = 0; q < EW / 2; q++) acc[a][q] = __ffma2_rn(xv[a], wv[q], acc[a][q]);
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();                          // staging memory free for the partials
+#pragma unroll
+    for (int a = 0; a < TW; a++)
+#pragma unroll
+        for (int q = 0; q < EW / 2; q++) {
+            float *pp = part + ((size_t)j * CT + tl0 + a) * CE + we * EW + 2 * q;
+            pp[0] = acc[a][q].x;
+            pp[1] = acc[a][q].y;
+        }
+    cluster_sync_all();
+    if (g == 0) {
+        for (int o = threadIdx.x; o < CT * CE; o += NT) {
+            const int tl = o / CE, el = o % CE;
+            float p[32];
+#pragma unroll
+            for (int l = 0; l < 32; l++) p[l] = ld_cluster_f32(part + ((size_t)(l % L) * CT + tl) * CE + el, l / L);
+#pragma unroll
+            for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+                for (int l = 0; l < h; l++) p[l] = p[l] + p[l + h];
+            const int t = t0 + tl, e = e0 + el;
+            if (t < T && e < E) {
+                float v = p[0];
+                if (bias) v = v + bias[e];
+                z[(size_t)t * E + e] = v;
+            }
+        }
+    }
+    cluster_sync_all();                       // the partials stay readable until CTA 0 is done
+    pdl_trigger();
+}
+
+template <int TW, int EW, int WT, int WE, int CH, int STAGES>
+static cudaError_t launch_gate_split_cfg(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T,
+                                         int d, int E, cudaStream_t st)
+{
+    constexpr int CT = TW * 4 * WT, CE = EW * WE, CC = CH / kGateSplit;
+    if (d % CH || E % 4) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)STAGES * (CT * (CC + 8) * 2 + CC * (CE + 4) * 4);
+    auto kern = gate_logits_split_kernel<TW, EW, WT, WE, CH, STAGES>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((T + CT - 1) / CT, (E + CE - 1) / CE, kGateSplit);
     return launch_pdl(kern, grid, dim3(WT * WE * 32), smem, st, x, gate_w, bias, z, T, d, E);
 }
 
@@ -331,8 +517,14 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
     // T=4096: 272 -> 234 us, T=16384 at d=7168: 1489 -> 1457 us against
     // 8 x 16 tiles of 6 x 2 warps); 4 x 16 tiles, 8 x 1 warps from 192 (T=512:
     // 60 -> 47 us); 4 x 8 tiles, 4 x 2 warps below.  256-channel chunks
-    // (fewer block barriers) where d allows, else 128 channels.
-    // E not a multiple of 4 loads gate_w by words.
+    // (fewer block barriers) where d allows, else 128 channels.  The largest and
+    // smallest shapes load each channel step's operands during the previous
+    // step's multiply-adds (T=128: 24.3 -> 22.7 us, T=16384: 1453 -> 1428 us).
+    // E not a multiple of 4 loads gate_w by words.  Batches whose 16 x 16 tiles
+    // would leave SMs idle split every logit's partial sums over clusters of
+    // four CTAs (T=40: 23 -> 17 us; E=64 at T=128: 23 -> 14 us).
+    if (E % 4 == 0 && d % 256 == 0 && (long long)((T + 15) / 16) * ((E + 15) / 16) < 128)
+        return launch_gate_split_cfg<2, 8, 1, 4, 256, 4>(x, gate_w, bias, z, T, d, E, st);
     if (E % 4) {
         return T >= 2048 ? launch_gate_cfg<8, 16, 4, 2, false>(x, gate_w, bias, z, T, d, E, st)
                          : launch_gate_cfg<4, 8, 4, 1, false>(x, gate_w, bias, z, T, d, E, st);
@@ -342,9 +534,9 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
         if (T >= 192) return launch_gate_cfg<4, 16, 8, 1, true, 128, 4>(x, gate_w, bias, z, T, d, E, st);
         return launch_gate_cfg<4, 8, 4, 1, true>(x, gate_w, bias, z, T, d, E, st);
     }
-    if (T >= 1536) return launch_gate_cfg<6, 16, 4, 2, true, 256, 2>(x, gate_w, bias, z, T, d, E, st);
+    if (T >= 1536) return launch_gate_cfg<6, 16, 4, 2, true, 256, 2, true>(x, gate_w, bias, z, T, d, E, st);
     if (T >= 192) return launch_gate_cfg<4, 16, 8, 1, true, 256, 3>(x, gate_w, bias, z, T, d, E, st);
-    return launch_gate_cfg<4, 8, 4, 2, true, 256, 3>(x, gate_w, bias, z, T, d, E, st);
+    return launch_gate_cfg<4, 8, 4, 2, true, 256, 3, true>(x, gate_w, bias, z, T, d, E, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -492,16 +684,19 @@ cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const 
 constexpr int kPlanWarps = 32;
 constexpr int kPlanPairsPerCta = 2048;
 constexpr int kPlanFusedChunk = 256;
+constexpr int kPlanFusedWarps = 8;      // one 32-pair step per warp
+constexpr long long kPlanFusedSmallPairs = 8192;
 constexpr long long kPlanFusedMaxPairs = 32768;
 
 // Count this CTA's pairs into the warp rows cnt[warp][e]; returns nothing,
 // flags out-of-range experts (treated as expert 0 so the plan stays a bijection).
+template <int NW>
 __device__ __forceinline__ void plan_count_warps(const int32_t *__restrict__ topk_idx, int *cnt, long long pb,
                                                  long long pe, int E, bool *bad)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long n = pe - pb;
-    const long long wchunk = (n + kPlanWarps - 1) / kPlanWarps;
+    const long long wchunk = (n + NW - 1) / NW;
     const long long wb = pb + warp * wchunk;
     const long long we = (wb + wchunk < pe) ? wb + wchunk : pe;
     int *my = cnt + warp * E;
@@ -529,7 +724,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_count_kernel(const int32
     const long long pb = (long long)blockIdx.x * kPlanPairsPerCta;
     const long long pe = (pb + kPlanPairsPerCta < P) ? pb + kPlanPairsPerCta : P;
     bool bad = false;
-    plan_count_warps(topk_idx, cnt, pb, pe, E, &bad);
+    plan_count_warps<kPlanWarps>(topk_idx, cnt, pb, pe, E, &bad);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int sum = 0;
@@ -541,7 +736,8 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_count_kernel(const int32
 }
 
 // cta_counts == NULL: a single CTA covers all pairs (no count kernel needed).
-__global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int32_t *__restrict__ topk_idx,
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) plan_scatter_kernel(const int32_t *__restrict__ topk_idx,
                                                                        const int *__restrict__ cta_counts,
                                                                        int32_t *__restrict__ expert_offsets,
                                                                        int32_t *__restrict__ sorted_pair,
@@ -556,7 +752,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
     pdl_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_tile_done; i += blockDim.x) tile_done[i] = 0;
-    extern __shared__ int cnt[];                  // [kPlanWarps][E]
+    extern __shared__ int cnt[];                  // [NW][E]
     __shared__ int tot[257];                      // per-expert total, then this CTA's first slot
     __shared__ int pre[257];                      // pairs of the expert in earlier CTAs
     __shared__ int tiles[257];
@@ -566,7 +762,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
     const int C = gridDim.x;
     // several CTAs and no count kernel: every CTA counts all pairs itself
     const bool fused = C > 1 && !cta_counts;
-    for (int i = threadIdx.x; i < kPlanWarps * E; i += blockDim.x) cnt[i] = 0;
+    for (int i = threadIdx.x; i < NW * E; i += blockDim.x) cnt[i] = 0;
     for (int i = threadIdx.x; i < E; i += blockDim.x) {
         tot[i] = 0;
         pre[i] = 0;
@@ -576,7 +772,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
     const long long pb = (long long)blockIdx.x * chunk;
     const long long pe = (pb + chunk < P) ? pb + chunk : P;
     bool bad = false;
-    plan_count_warps(topk_idx, cnt, pb, pe, E, &bad);
+    plan_count_warps<NW>(topk_idx, cnt, pb, pe, E, &bad);
     if (fused) {
         // per-expert totals and pairs before this chunk (order-free counts);
         // four 16-byte index loads in flight per thread
@@ -621,7 +817,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
                 total += v;
             }
         } else {
-            for (int w = 0; w < kPlanWarps; w++) total += cnt[w * E + e];
+            for (int w = 0; w < NW; w++) total += cnt[w * E + e];
         }
         tot[e] = total;
         pre[e] = before;
@@ -665,7 +861,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
     // each warp's first slot per expert
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = tot[e];
-        for (int w = 0; w < kPlanWarps; w++) {
+        for (int w = 0; w < NW; w++) {
             const int c = cnt[w * E + e];
             cnt[w * E + e] = run;
             run += c;
@@ -674,7 +870,7 @@ __global__ void __launch_bounds__(kPlanWarps * 32) plan_scatter_kernel(const int
     __syncthreads();
 
     const long long n = pe - pb;
-    const long long wchunk = (n + kPlanWarps - 1) / kPlanWarps;
+    const long long wchunk = (n + NW - 1) / NW;
     const long long wb = pb + warp * wchunk;
     const long long we = (wb + wchunk < pe) ? wb + wchunk : pe;
     int *my = cnt + warp * E;
@@ -725,19 +921,33 @@ cudaError_t launch_plan(const int32_t *topk_idx, int32_t *expert_offsets, int32_
     const int G4 = xs_tiles ? stage_groups(d) : 0;
     const long long P = (long long)T * k;
     const size_t smem = (size_t)kPlanWarps * E * sizeof(int);
+    const size_t smem_small = (size_t)kPlanFusedWarps * E * sizeof(int);
     const long long C = (P + kPlanPairsPerCta - 1) / kPlanPairsPerCta;
     if (P <= kPlanFusedMaxPairs || !cta_counts) {
         // one kernel: kPlanFusedChunk pairs per CTA up to kPlanFusedMaxPairs
         // pairs; one CTA for all pairs beyond that when there is no scratch
-        const long long CF = P <= kPlanFusedMaxPairs ? std::max(1LL, (P + kPlanFusedChunk - 1) / kPlanFusedChunk) : 1;
-        return launch_pdl(plan_scatter_kernel, dim3((unsigned)CF), dim3(kPlanWarps * 32), smem, st, topk_idx,
+        if (P <= kPlanFusedMaxPairs) {
+            const long long CF = std::max(1LL, (P + kPlanFusedChunk - 1) / kPlanFusedChunk);
+            // eight warps (one 32-pair step each, cheaper block barriers) while
+            // every CTA's count of all pairs stays short; 32 beyond that
+            if (P <= kPlanFusedSmallPairs)
+                return launch_pdl(plan_scatter_kernel<kPlanFusedWarps>, dim3((unsigned)CF), dim3(kPlanFusedWarps * 32),
+                                  smem_small, st, topk_idx, (const int *)nullptr, expert_offsets, sorted_pair,
+                                  pair_pos, tile_prefix, P, E, status, xs, xs_stride, xs_tiles, G4, k, tile_rows,
+                                  tile_done, n_tile_done, kPlanFusedChunk);
+            return launch_pdl(plan_scatter_kernel<kPlanWarps>, dim3((unsigned)CF), dim3(kPlanWarps * 32), smem, st,
+                              topk_idx, (const int *)nullptr, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E,
+                              status, xs, xs_stride, xs_tiles, G4, k, tile_rows, tile_done, n_tile_done,
+                              kPlanFusedChunk);
+        }
+        return launch_pdl(plan_scatter_kernel<kPlanWarps>, dim3(1), dim3(kPlanWarps * 32), smem, st, topk_idx,
                           (const int *)nullptr, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs,
                           xs_stride, xs_tiles, G4, k, tile_rows, tile_done, n_tile_done, kPlanFusedChunk);
     }
     cudaError_t err = launch_pdl(plan_count_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                                  cta_counts, P, E, status);
     if (err != cudaSuccess) return err;
-    return launch_pdl(plan_scatter_kernel, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
+    return launch_pdl(plan_scatter_kernel<kPlanWarps>, dim3((unsigned)C), dim3(kPlanWarps * 32), smem, st, topk_idx,
                       (const int *)cta_counts, expert_offsets, sorted_pair, pair_pos, tile_prefix, P, E, status, xs,
                       xs_stride, xs_tiles, G4, k, tile_rows, tile_done, n_tile_done, kPlanPairsPerCta);
 }

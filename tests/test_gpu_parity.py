@@ -147,6 +147,7 @@ def test_quantize_act_bitexact():
     (40, 384, 16, 4, False, False),       # small batch, 128-channel chunks
     (300, 384, 32, 4, False, True),       # mid batch, 128-channel chunks
     (1540, 256, 40, 4, False, False),     # large batch, E not a multiple of the CTA's 32 experts
+    (37, 512, 40, 4, True, True),         # partial sums split over CTA clusters; ragged T, partial expert tile
 ])
 def test_route_bitexact(T, d, E, k, ties, bias):
     rng = np.random.default_rng(T * 31 + E)
