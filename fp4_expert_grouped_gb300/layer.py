@@ -76,3 +76,56 @@ def forward(x: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
     if routing:
         return out, ti, tw, pp
     return out
+
+
+class GraphedForward:
+    """A serving step captured once as a CUDA graph and replayed per step: copy
+    the step's tokens in from pinned host memory, run the layer forward,
+    copy the output back to pinned host memory.
+
+    The captured work is exactly that of ``forward`` (the same kernels, with
+    programmatic dependent launch between them kept as graph edges), on
+    device buffers owned by this object.  Replaying costs the host one graph
+    launch instead of the argument marshalling and the per-kernel launches of
+    an eager call, which matters when every step waits for its result (a
+    decode loop).  Inputs are read from ``x_host`` at replay time: write the
+    next step's tokens into it, then call ``replay``; ``out_host`` holds the
+    result once the stream reaches the end of the replay.
+    """
+
+    def __init__(self, x_host: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
+                 gate_bias: Optional[torch.Tensor] = None, out_host: Optional[torch.Tensor] = None):
+        if not x_host.is_pinned():
+            raise ValueError("x_host must be pinned host memory")
+        dev = gate_w.device
+        T, d = x_host.shape
+        E = gate_w.shape[1]
+        inter = pk.w13_fp4.shape[1] // 2
+        self.x_host = x_host
+        self.out_host = out_host if out_host is not None else torch.empty_like(x_host).pin_memory()
+        if not self.out_host.is_pinned() or self.out_host.shape != x_host.shape:
+            raise ValueError("out_host must be pinned host memory shaped like x_host")
+        self.x = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
+        self.out = torch.empty_like(self.x)
+        self.ws = workspace(T, d, inter, E, k, dev)
+        self._args = (gate_w, pk, k, gate_bias)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self._body()                      # eager once: kernel attributes set outside the capture
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            self._body()
+
+    def _body(self):
+        gate_w, pk, k, gate_bias = self._args
+        self.x.copy_(self.x_host, non_blocking=True)
+        capi.moe_forward_ex(self.x, gate_w, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, self.out, k,
+                            gate_bias=gate_bias, workspace=self.ws)
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def replay(self):
+        """Enqueue one step on the current stream."""
+        self.graph.replay()
