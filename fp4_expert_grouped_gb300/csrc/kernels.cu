@@ -567,33 +567,42 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ zt, int32_t 
         }
         v[m] = val;
     }
-    uint32_t taken = 0;
+    // Selection on 64-bit keys: the logit's bits mapped to an unsigned order
+    // (-0 taken as +0, so equal logits compare equal), then the inverted expert
+    // index, so the larger key is the larger logit and, among equal logits,
+    // the lower expert.  Each round is one max over the lane's keys and a
+    // 5-step butterfly; the winner's owner clears its key.
+    uint64_t key[8];
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+        const int e = lane + 32 * m;
+        uint64_t kk = 0;
+        if (e < E) {
+            const uint32_t u = __float_as_uint(v[m] + 0.0f);
+            const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+            kk = ((uint64_t)o << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+        }
+        key[m] = kk;
+    }
     float my_z = 0.f;
     int my_e = 0;
     for (int j = 0; j < k; j++) {
-        float bz = -INFINITY;
-        int be = INT_MAX;
+        uint64_t best = key[0];
 #pragma unroll
-        for (int m = 0; m < 8; m++) {
-            const int e = lane + 32 * m;
-            if (e < E && !((taken >> m) & 1u) && (v[m] > bz || (v[m] == bz && e < be))) {
-                bz = v[m];
-                be = e;
-            }
-        }
+        for (int m = 1; m < 8; m++) best = key[m] > best ? key[m] : best;
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {
-            const float oz = __shfl_xor_sync(0xffffffffu, bz, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (oz > bz || (oz == bz && oe < be)) {
-                bz = oz;
-                be = oe;
-            }
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const int e = (int)(0xFFFFFFFFu - (uint32_t)best);
+        const bool mine = (e & 31) == lane;
+#pragma unroll
+        for (int m = 0; m < 8; m++) key[m] = (mine && m == (e >> 5)) ? 0ull : key[m];
         if (lane == j) {
-            my_z = bz;
-            my_e = be;
+            const uint32_t o = (uint32_t)(best >> 32);
+            my_z = __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+            my_e = e;
         }
     }
     if (bad && lane == 0) flag_status(status, kStatusBadData);
@@ -628,7 +637,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float *__re
     uint8_t *qrow = xq + (size_t)t * d;
     uint8_t *srow = xs + (size_t)t * xs_stride;
     const int G = d / 128;
-    for (int g = warp; g < G; g += kTopkWarps) {
+    // warp 0 selects; the other warps quantise
+    for (int g = warp - 1; warp > 0 && g < G; g += kTopkWarps - 1) {
         const int e = quant_group_warp(xrow + g * 128, qrow + g * 128);
         if (lane == 0) srow[g] = (uint8_t)(e + 127);
     }
