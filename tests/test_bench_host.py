@@ -29,6 +29,21 @@ def test_flop_identity_matches_cited_ratio():
     assert bench.gemm_flops(w, "gemm1") + bench.gemm_flops(w, "gemm2") == flops
 
 
+def test_kernels_per_step_follow_the_library_thresholds():
+    """gpu_launches claim: gate, top-k, plan (one kernel up to 32768 pairs, a
+    count and a scatter kernel above), the expert-ordered copy (from 16 pairs
+    per expert on average), GEMM1, GEMM2, combine."""
+    want = {"tiny": 6, "decode": 6, "mid": 7, "skew": 8, "prefill": 8}
+    for name, n in want.items():
+        assert bench.kernels_per_step(inputs.WORKLOADS[name]) == n, name
+    edge = inputs.Workload("edge", T=4096, d=256, inter=128, E=256, k=8, seed=0)    # 32768 pairs: one plan kernel
+    assert bench.kernels_per_step(edge) == 7
+    edge = inputs.Workload("edge", T=4097, d=256, inter=128, E=256, k=8, seed=0)    # 32776 pairs: two
+    assert bench.kernels_per_step(edge) == 8
+    edge = inputs.Workload("edge", T=511, d=256, inter=128, E=256, k=8, seed=0)     # 4088 < 16 E: no copy
+    assert bench.kernels_per_step(edge) == 6
+
+
 def test_weight_bytes_per_expert():
     assert bench.weight_bytes_per_expert(4096, 2048) == 13_369_344
     assert bench.weight_bytes_per_expert(7168, 2048) == 23_396_352
