@@ -251,7 +251,7 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     moe_forward_opts o;
     std::memset(&o, 0, sizeof o);
     if (opts) o = *opts;
-    if (o.flags != 0) return MOE_ERR_INVALID_ARG;
+    if (o.flags & ~MOE_FLAG_TEST_STALL_GEMM2) return MOE_ERR_INVALID_ARG;
     if (o.gate_bias && !aligned(o.gate_bias, 4)) return MOE_ERR_INVALID_ARG;
     if ((o.topk_idx_out && !aligned(o.topk_idx_out, 4)) || (o.topk_w_out && !aligned(o.topk_w_out, 4)) ||
         (o.pair_pos_out && !aligned(o.pair_pos_out, 4)))
@@ -353,6 +353,7 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
         g.N = d;
         g.K = inter;
         g.y = y;
+        g.stall_test = (o.flags & MOE_FLAG_TEST_STALL_GEMM2) ? 1 : 0;
         e = launch_gemm2(g, d, s);
     }
     mark(MOE_STAGE_COMBINE);

@@ -78,8 +78,9 @@ struct Cfg {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_AMAX = OFF_SFB + STAGES * SFB_STAGE;          // [2 tile parities][2 halves][128 rows] fp32
     static constexpr int OFF_BAR = OFF_AMAX + 2 * 2 * BM * 4;
-    // full, empty, sf_ready per stage; acc_full, acc_empty; one amax-exchange barrier per lane quarter
-    static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 2 + 4) * 8;
+    // full, empty, sf_ready per stage; acc_full, acc_empty; one amax-exchange
+    // barrier per lane quarter; two for the exit drain (MMA thread, scale warp)
+    static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 2 + 4 + 2) * 8;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static constexpr int SMEM_USED = OFF_PLAN + 2 * PLAN_INTS * 4;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
     uint64_t *acc_full = full + 3 * STAGES;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *xbar = acc_empty + 1;            // [4] amax exchange of the two epilogue warps of a lane quarter
+    uint64_t *drain = xbar + 4;                // [2] exit: MMA thread's, scale warp's tensor-core work done
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
     int *s_offs = reinterpret_cast<int *>(smem + OFF_PLAN);
@@ -181,6 +183,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
         // 16-row tiles: only the two epilogue warps of lane quarter 0 hold rows
         mbar_init(acc_empty, TR == 16 ? 64 : EPI_WARPS * 32);
         for (int i = 0; i < 4; i++) mbar_init(&xbar[i], 64);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
         // (Prefetching B into L2 ahead of the ring was measured and made every
         // workload slower.)
         uint32_t stage = 0, phase = 0;
+        long long armed = 0;                                // stages armed so far (exit drain)
         const int ga = stage_groups(g.K);                   // activation scale groups per tile
         bool gemm1_done = false;                            // GEMM2: all of GEMM1's tiles published
         for (long long tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
@@ -263,11 +268,14 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             // first look at the total usually says so, costing one load per CTA)
             if (MODE == 2 && !gemm1_done) {
                 const int per_tile = (TR == 16 ? 2 : EPI_WARPS) * (g.K / 128);
+                // (test flag: a count GEMM1 never reaches, so the wait runs out
+                // before this CTA issues any copy)
                 if (lane == 0) {
-                    if (ld_acquire(g.all_done) >= per_tile * s_tp[E]) {
+                    if (!g.stall_test && ld_acquire(g.all_done) >= per_tile * s_tp[E]) {
                         gemm1_done = true;
                         fence_proxy_async_global();
-                    } else if (wait_counter(g.tile_done + ti.m_tile, per_tile, tmo, abort_flag)) {
+                    } else if (wait_counter(g.tile_done + ti.m_tile, per_tile + (g.stall_test ? 1 : 0), tmo,
+                                            abort_flag)) {
                         fence_proxy_async_global();
                     } else {
                         *abort_flag = 1;
@@ -295,6 +303,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 uint8_t *sa = smem + OFF_A + stage * A_STAGE;
                 uint8_t *sb = smem + OFF_B + stage * B_STAGE;
                 uint64_t *fb = &full[stage];
+                armed++;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, stage_tx + ((ks & 3) == 0 ? SFA_STAGE : 0));
                     if (dense) tma_load_2d(sa, dense_small ? &tmA3 : &tmA2, fb, ks * BK, ti.row0);
@@ -323,6 +332,17 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 }
             }
         }
+        // Leave no copy of this CTA in flight: wait for the last use of every
+        // slot armed so far (already complete unless a wait above gave up).
+        // Slots below `stage` were last armed in this lap of the ring, the
+        // others in the previous one.
+        if (lane == 0) {
+            for (int s = 0; s < STAGES; s++) {
+                if (armed <= s) continue;
+                mbar_wait_drain(&full[s], s < (int)stage ? phase : (phase ^ 1u), tmo);
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         uint32_t stage = 0, phase = 0, acc_phase = 0;
@@ -380,6 +400,12 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             __syncwarp();
             acc_phase ^= 1u;
         }
+        // tensor memory is freed below: let this thread's MMAs and copies finish
+        if (lane == 0) {
+            tc_commit(&drain[0]);
+            mbar_wait_drain(&drain[0], 0, tmo);
+        }
+        __syncwarp();
     } else if (SFW && warp == SF_WARP) {
         // ------------------------------------------------------- B scale factors
         // Same tile and stage walk as the MMA warp: once a stage is full, copy
@@ -413,6 +439,11 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             }
         }
         if (!ok) *abort_flag = 1;
+        if (lane == 0) {
+            tc_commit(&drain[1]);
+            mbar_wait_drain(&drain[1], 0, tmo);
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         // Eight warps: warp w reads tensor-memory lanes 32 * (w % 4) ..; the two

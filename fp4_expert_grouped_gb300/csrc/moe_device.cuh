@@ -105,6 +105,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// Bounded wait that ignores the abort flag: used on the way out to let this
+// CTA's own copies and tensor-core operations finish before it exits.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t timeout_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    return true;
+}
+
 // 32-byte global store (address 32-byte aligned): a whole L2 sector per lane,
 // half the store instructions of 16-byte vectors.
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8])

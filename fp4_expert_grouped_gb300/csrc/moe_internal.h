@@ -173,6 +173,9 @@ struct GemmArgs {
     unsigned *status;
     unsigned long long timeout_ns;
     int num_sms;
+    // GEMM2, tests only: wait for a GEMM1 count that never comes (before any
+    // copy), so the bounded wait expires
+    int stall_test;
 };
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st);
 cudaError_t launch_gemm2(const GemmArgs &a, int d, cudaStream_t st);

@@ -189,12 +189,20 @@ typedef struct moe_forward_opts {
     int32_t *topk_idx_out;     /* optional device copies of the routing: [T][k] */
     float *topk_w_out;         /* [T][k] */
     int32_t *pair_pos_out;     /* [T*k] position of pair t*k+j in expert order */
-    uint32_t flags;            /* must be 0 */
+    uint32_t flags;            /* 0, or MOE_FLAG_TEST_STALL_GEMM2 (tests only) */
     void **stage_events;       /* optional: MOE_STAGE_COUNT + 1 caller-created
                                   cudaEvent_t, recorded on the stream before the
                                   first stage, between stages and after the last
                                   (per-stage timing); NULL = none */
 } moe_forward_opts;
+
+/* Test only (failure detection without a GPU fault): GEMM2 waits for a
+ * GEMM1 completion count that is never published, before it issues any copy.
+ * Its bounded wait (FP4MOE_TIMEOUT_MS, default 2000 ms) runs out, every CTA
+ * leaves through its exit path, and moe_get_device_status then reports
+ * MOE_ERR_TIMEOUT.  The output of that call is not computed; the next call
+ * runs normally. */
+#define MOE_FLAG_TEST_STALL_GEMM2 0x1u
 
 /* Stages of moe_forward_ex, in launch order (index into stage_events). */
 enum {

@@ -69,7 +69,7 @@ def test_forward_argument_checks(capi):
     assert fwd(lib, E=300) == SHAPE
     assert fwd(lib, T=1 << 28, k=8) == SHAPE                # T*k >= 2^31
     o = capi.MoeForwardOpts()
-    o.flags = 1
+    o.flags = 2                                             # no such flag
     assert fwd(lib, opts=o) == INV
     o = capi.MoeForwardOpts()
     o.workspace = FAKE
