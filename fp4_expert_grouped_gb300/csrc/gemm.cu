@@ -29,7 +29,7 @@
 //               A's scale factors -> tensor memory (tcgen05.cp, every fourth
 //               stage), then 4 MMAs of K = 32 per stage into a 128 x 256 fp32
 //               accumulator
-//   warp 10     (16-row tiles) B's scale factors -> tensor memory, one copy
+//   warp 10     (16/32-row tiles) B's scale factors -> tensor memory, one copy
 //               pair per stage; otherwise the MMA thread copies them
 //   warps 2-9   epilogue, two warps per 32-lane quarter of tensor memory, each
 //               with half of the columns: tcgen05.ld to registers, release of
@@ -53,23 +53,24 @@ constexpr int SFB_STAGE = 1024;           // 256 rows x 4 bytes
 constexpr int B_STAGE = BN * BK;          // 32 KB: 256 rows x 128 codes, one byte per code in shared memory
 constexpr int PLAN_INTS = 260;
 constexpr int EPI_WARPS = 8;              // two warps per 32-lane quarter of tensor memory
-constexpr int SF_WARP = 2 + EPI_WARPS;    // B scale-factor copies into tensor memory (16-row tiles)
+constexpr int SF_WARP = 2 + EPI_WARPS;    // B scale-factor copies into tensor memory (16/32-row tiles)
 
 // Shared-memory layout per tile size TR (pair rows per tile).  TR = 128: a
 // 4-stage ring of 48 KB stages (A 16 KB, B 32 KB).  TR = 16: A slots of 2 KB
-// and a 6-stage ring (50% more weight bytes in flight).  The MMA always reads
-// 128 A rows (16 KB) from a slot's start; with 2 KB slots the rows past 16
-// come from whatever follows the slot in shared memory and only feed
-// accumulator rows that are discarded.  The A slots therefore come first.
+// and a 6-stage ring (50% more weight bytes in flight); TR = 32: 4 KB slots,
+// 5 stages (a sixth does not fit).  The MMA always reads 128 A rows (16 KB)
+// from a slot's start; with smaller slots the rows past TR come from whatever
+// follows the slot in shared memory and only feed accumulator rows that are
+// discarded.  The A slots therefore come first.
 template <int TR>
 struct Cfg {
-    static constexpr int STAGES = TR == 16 ? 6 : 4;
-    // 16-row tiles stream weights through a 6-deep ring: a separate warp copies
+    static constexpr int STAGES = TR == 16 ? 6 : TR == 32 ? 5 : 4;
+    // 16/32-row tiles stream weights through a deep ring: a separate warp copies
     // B's scale factors into tensor memory, keeping the MMA thread's per-stage
     // issue work under the stage's MMA time (decode GEMM1 363 -> 352 us).  With
     // 128-row tiles and a 4-deep ring the extra hop's latency cost more (large
     // batches 1-3% slower), so there the MMA thread copies them itself.
-    static constexpr bool SF_WARP = TR == 16;
+    static constexpr bool SF_WARP = TR <= 32;
     static constexpr int NUM_THREADS = (SF_WARP ? 3 + EPI_WARPS : 2 + EPI_WARPS) * 32;
     static constexpr int A_STAGE = TR * BK;
     static constexpr int OFF_A = 0;
@@ -84,7 +85,8 @@ struct Cfg {
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static constexpr int SMEM_USED = OFF_PLAN + 2 * PLAN_INTS * 4;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
-        static_assert((STAGES - 1) * A_STAGE + BM * BK <= SMEM_USED, "MMA A reads stay in shared memory");
+    static_assert((STAGES - 1) * A_STAGE + BM * BK <= SMEM_USED, "MMA A reads stay in shared memory");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
@@ -180,8 +182,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             mbar_init(&sf_ready[s], 1);
         }
         mbar_init(acc_full, 1);
-        // 16-row tiles: only the two epilogue warps of lane quarter 0 hold rows
-        mbar_init(acc_empty, TR == 16 ? 64 : EPI_WARPS * 32);
+        // 16/32-row tiles: only the two epilogue warps of lane quarter 0 hold rows
+        mbar_init(acc_empty, TR <= 32 ? 64 : EPI_WARPS * 32);
         for (int i = 0; i < 4; i++) mbar_init(&xbar[i], 64);
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             // and [d/2 + 128 t, +128)) are adjacent blocks of the tiled layout,
             // pair t: blocks blk + 2 ks and blk + 2 ks + 1.
             const long long blk = weight_block(ti.e, ti.n_block, 0, g.N, g.K);
-            const bool small = TR == 16 || ti.valid <= SMALL_TILE_ROWS;   // 16-row tiles: always 16-row boxes
+            const bool small = TR <= 32 || ti.valid <= SMALL_TILE_ROWS;   // 16/32-row tiles: always 16-row boxes
             const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
             // GEMM1: a dense tile reads its rows from the expert-ordered copy, a
             // sparse one gathers them (four rows per TMA gather)
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             // (once GEMM1 has finished altogether no tile needs to wait: the
             // first look at the total usually says so, costing one load per CTA)
             if (MODE == 2 && !gemm1_done) {
-                const int per_tile = (TR == 16 ? 2 : EPI_WARPS) * (g.K / 128);
+                const int per_tile = (TR <= 32 ? 2 : EPI_WARPS) * (g.K / 128);
                 // (test flag: a count GEMM1 never reaches, so the wait runs out
                 // before this CTA issues any copy)
                 if (lane == 0) {
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
         const int r = q * 32 + lane;               // accumulator row = pair row in the tile
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL;
         uint32_t acc_phase = 0, tpar = 0;
-        // 16-row tiles have no rows in lane quarters 1-3
+        // 16- and 32-row tiles have no rows in lane quarters 1-3
         for (long long tile = blockIdx.x; (TR == 128 || q == 0) && tile < total_tiles && !*abort_flag;
              tile += gridDim.x) {
             const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb, TR);
@@ -638,19 +640,26 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
         return cudaErrorInvalidValue;
     }
     if (!make_map_b(&mb, a.b, (long long)a.E * (a.N / 128) * (a.K / 128))) return cudaErrorInvalidValue;
+    const bool dense = MODE == 1 && a.a_dense;
     auto kern = gg::grouped_gemm_kernel<MODE, false, 128>;
     int smem = gg::Cfg<128>::SMEM_BYTES;
+    int threads = gg::Cfg<128>::NUM_THREADS;
     if (a.tile_rows == 16) {
+        if (dense) return cudaErrorInvalidValue;   // the copy exists from 16 pairs per expert on
         kern = gg::grouped_gemm_kernel<MODE, false, 16>;
         smem = gg::Cfg<16>::SMEM_BYTES;
-    } else if (a.tile_rows != 128) {
+        threads = gg::Cfg<16>::NUM_THREADS;
+    } else if (a.tile_rows == 32) {
+        kern = gg::grouped_gemm_kernel<MODE, false, 32>;
+        smem = gg::Cfg<32>::SMEM_BYTES;
+        threads = gg::Cfg<32>::NUM_THREADS;
+        if constexpr (MODE == 1)
+            if (dense) kern = gg::grouped_gemm_kernel<1, true, 32>;
+    } else if (a.tile_rows == 128) {
+        if constexpr (MODE == 1)
+            if (dense) kern = gg::grouped_gemm_kernel<1, true, 128>;
+    } else {
         return cudaErrorInvalidValue;
-    }
-    if constexpr (MODE == 1) {
-        if (a.a_dense) {
-            if (a.tile_rows != 128) return cudaErrorInvalidValue;
-            kern = gg::grouped_gemm_kernel<1, true, 128>;
-        }
     }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
@@ -658,7 +667,6 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
     if (!(MODE == 1 && a.a_dense)) ma3 = ma2;   // unused
-    const int threads = a.tile_rows == 16 ? gg::Cfg<16>::NUM_THREADS : gg::Cfg<128>::NUM_THREADS;
     return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ma, ma2, ma3, mb, a, out_dim);
 }
 

@@ -66,12 +66,17 @@ inline int scale_row_stride(int channels) { return ((channels / 128) + 3) / 4 * 
 
 // upper bound on the number of 128-row tiles of the expert-ordered pairs
 // Pair rows per GEMM row tile: 16 for batches averaging at most 8 pairs per
-// expert, 128 otherwise.  A small batch's tiles hold a few rows each, and the
-// shared memory a 128-row A slot takes is better spent on a deeper ring of
-// weight stages (the GEMMs then stream weights at ~90% of HBM bandwidth
-// instead of ~80%).  The MMA still computes 128 rows; rows past the tile's
-// own are discarded, so a row's result does not depend on the tile size.
-__host__ __device__ inline int gemm_tile_rows(long long P, int E) { return P <= 8LL * E ? 16 : kTileM; }
+// expert, 32 up to 20 (an expert's pair count is then above 32 for about one
+// expert in 200, which then streams its weights twice), 128 otherwise.  A
+// small batch's tiles hold a few rows each, and the shared memory a 128-row A
+// slot takes is better spent on a deeper ring of weight stages (the GEMMs
+// then stream weights at ~90% of HBM bandwidth instead of ~80%).  The MMA
+// still computes 128 rows; rows past the tile's own are discarded, so a row's
+// result does not depend on the tile size.
+__host__ __device__ inline int gemm_tile_rows(long long P, int E)
+{
+    return P <= 8LL * E ? 16 : P <= 20LL * E ? 32 : kTileM;
+}
 
 // Upper bound of the row tiles of all experts: every expert's last tile may
 // be partial.

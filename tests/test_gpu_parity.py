@@ -6,6 +6,8 @@ relative L2 <= 5e-3): the layer output.  Plus determinism (repeated calls give
 identical bits) and batch invariance (a token's output bits do not depend on
 the rest of the batch).  Every test here needs a GB300.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -238,6 +240,9 @@ def test_forward_tiny_all_tokens():
     (2100, 256, 128, 13, 3, True),       # large-batch gate kernel: ragged T, odd E
     (48, 256, 128, 16, 2, True),         # 16-row tiles: experts of 16 and 17 pairs (a 1-row tail tile), empty experts
     (60, 512, 128, 8, 1, True),          # 16-row tiles, k = 1, one expert spanning two tiles
+    (60, 256, 128, 8, 2, False),         # 32-row tiles, every A row gathered (under 16 pairs per expert)
+    (76, 512, 256, 8, 2, True),          # 32-row tiles with the expert-ordered copy; biased: experts over 32 pairs
+    (150, 256, 128, 16, 2, True),        # 32-row tiles with the copy, ragged tails and empty experts
 ])
 def test_forward_small_shapes(T, d, inter, E, k, bias):
     w, x, gw, b, w13, w2 = small_case(T, d, inter, E, k, seed=T + d, bias=bias)
@@ -287,18 +292,31 @@ def workload_cache():
     return {}
 
 
+def _named_workload(name):
+    """The benchmark's workloads, plus "decode<T>": the decode layer (same
+    seed, so the same experts) at a batch of T tokens."""
+    if name in inputs.WORKLOADS:
+        return inputs.WORKLOADS[name]
+    assert name.startswith("decode")
+    return dataclasses.replace(inputs.WORKLOADS["decode"], name=name, T=int(name[len("decode"):]))
+
+
 def _workload(name, cache):
     if name not in cache:
+        w = _named_workload(name)
+        key = (w.seed, w.E, w.d, w.inter)
+        pk = cache.get("pk") if cache.get("pk_key") == key else None
         cache.clear()
         torch.cuda.empty_cache()
-        w = inputs.WORKLOADS[name]
         x, gw, b = inputs.make_x_gate(w, DEV)
-        pk = layer().pack_workload(w, DEV)
+        if pk is None:
+            pk = layer().pack_workload(w, DEV)
         cache[name] = (w, x, gw, b, pk)
+        cache["pk"], cache["pk_key"] = pk, key
     return cache[name]
 
 
-@pytest.mark.parametrize("name", ["decode", "mid", "skew", "prefill"])
+@pytest.mark.parametrize("name", ["decode", "decode384", "decode512", "mid", "skew", "prefill"])
 def test_forward_full_size_sampled_tokens(name, workload_cache):
     """Full-size workloads in the benchmark's launch configuration; the oracle
     recomputes a seeded sample of tokens (every token is independent)."""
@@ -370,7 +388,7 @@ def test_workspace_intermediates_tiny():
     f2, s2 = oracle.pack_fp4(w2.numpy())
     hq = wsn[off[c.MOE_WS_HQ]:][:w.P * w.inter].reshape(w.P, w.inter)
     tp = wsn[off[c.MOE_WS_TILE_PREFIX]:][:4 * (w.E + 1)].view(np.int32)
-    R = 16 if w.P <= 8 * w.E else 128          # pair rows per GEMM row tile
+    R = 16 if w.P <= 8 * w.E else 32 if w.P <= 20 * w.E else 128    # pair rows per GEMM row tile
     assert np.array_equal(tp, np.concatenate([[0], np.cumsum((np.diff(offs) + R - 1) // R)]))
     hs_tiles = wsn[off[c.MOE_WS_HS_TILES]:]
     GH = (w.inter // 128 + 3) // 4
