@@ -29,7 +29,7 @@
 //               A's scale factors -> tensor memory (tcgen05.cp, every fourth
 //               stage), then 4 MMAs of K = 32 per stage into a 128 x 256 fp32
 //               accumulator
-//   warp 10     (16/32-row tiles) B's scale factors -> tensor memory, one copy
+//   warp 10     (16/32/64-row tiles) B's scale factors -> tensor memory, one copy
 //               pair per stage; otherwise the MMA thread copies them
 //   warps 2-9   epilogue, two warps per 32-lane quarter of tensor memory, each
 //               with half of the columns: tcgen05.ld to registers, release of
@@ -53,24 +53,27 @@ constexpr int SFB_STAGE = 1024;           // 256 rows x 4 bytes
 constexpr int B_STAGE = BN * BK;          // 32 KB: 256 rows x 128 codes, one byte per code in shared memory
 constexpr int PLAN_INTS = 260;
 constexpr int EPI_WARPS = 8;              // two warps per 32-lane quarter of tensor memory
-constexpr int SF_WARP = 2 + EPI_WARPS;    // B scale-factor copies into tensor memory (16/32-row tiles)
+constexpr int SF_WARP = 2 + EPI_WARPS;    // B scale-factor copies into tensor memory (16/32/64-row tiles)
 
 // Shared-memory layout per tile size TR (pair rows per tile).  TR = 128: a
 // 4-stage ring of 48 KB stages (A 16 KB, B 32 KB).  TR = 16: A slots of 2 KB
-// and a 6-stage ring (50% more weight bytes in flight); TR = 32: 4 KB slots,
-// 5 stages (a sixth does not fit).  The MMA always reads 128 A rows (16 KB)
+// and a 6-stage ring (50% more weight bytes in flight); TR = 32 and 64: 4 and
+// 8 KB slots, 5 stages (a sixth does not fit).  The MMA always reads 128 A rows (16 KB)
 // from a slot's start; with smaller slots the rows past TR come from whatever
 // follows the slot in shared memory and only feed accumulator rows that are
 // discarded.  The A slots therefore come first.
 template <int TR>
 struct Cfg {
-    static constexpr int STAGES = TR == 16 ? 6 : TR == 32 ? 5 : 4;
+    static constexpr int STAGES = TR == 16 ? 6 : TR <= 64 ? 5 : 4;
     // 16/32-row tiles stream weights through a deep ring: a separate warp copies
     // B's scale factors into tensor memory, keeping the MMA thread's per-stage
     // issue work under the stage's MMA time (decode GEMM1 363 -> 352 us).  With
     // 128-row tiles and a 4-deep ring the extra hop's latency cost more (large
     // batches 1-3% slower), so there the MMA thread copies them itself.
-    static constexpr bool SF_WARP = TR <= 32;
+    static constexpr bool SF_WARP = TR <= 64;
+    // 32-lane quarters of tensor memory holding the tile's rows (the
+    // epilogue warps of the others have nothing to do)
+    static constexpr int EPI_Q = TR >= 128 ? 4 : (TR + 31) / 32;
     static constexpr int NUM_THREADS = (SF_WARP ? 3 + EPI_WARPS : 2 + EPI_WARPS) * 32;
     static constexpr int A_STAGE = TR * BK;
     static constexpr int OFF_A = 0;
@@ -182,8 +185,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             mbar_init(&sf_ready[s], 1);
         }
         mbar_init(acc_full, 1);
-        // 16/32-row tiles: only the two epilogue warps of lane quarter 0 hold rows
-        mbar_init(acc_empty, TR <= 32 ? 64 : EPI_WARPS * 32);
+        // small tiles: only the epilogue warps of the lane quarters holding rows
+        mbar_init(acc_empty, C::EPI_Q * 64);
         for (int i = 0; i < 4; i++) mbar_init(&xbar[i], 64);
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
@@ -246,18 +249,22 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             // and [d/2 + 128 t, +128)) are adjacent blocks of the tiled layout,
             // pair t: blocks blk + 2 ks and blk + 2 ks + 1.
             const long long blk = weight_block(ti.e, ti.n_block, 0, g.N, g.K);
-            const bool small = TR <= 32 || ti.valid <= SMALL_TILE_ROWS;   // 16/32-row tiles: always 16-row boxes
+            const bool small = TR <= 64 || ti.valid <= SMALL_TILE_ROWS;   // 16/32/64-row tiles: always 16-row boxes
             const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
             // GEMM1: a dense tile reads its rows from the expert-ordered copy, a
             // sparse one gathers them (four rows per TMA gather)
             const bool dense = DENSE && ti.valid > kDenseTileRows;
             // a dense tile of at most 32 rows loads one 32-row box of the copy,
-            // a larger one one 128-row box: one TMA request either way (the
-            // requests, not the bytes, are what an A stage costs)
-            const bool dense_small = dense && ti.valid <= kDenseBoxRows;
+            // a larger 128-row tile one 128-row box: one TMA request either way
+            // (the requests, not the bytes, are what an A stage costs); a
+            // 64-row tile of more than 32 rows two 32-row boxes (its A slot
+            // holds 64 rows)
+            const bool dense_big = dense && TR == 128 && ti.valid > kDenseBoxRows;
+            const int dense_boxes = dense && !dense_big ? (ti.valid + kDenseBoxRows - 1) / kDenseBoxRows : 0;
             const int a_gathers = (MODE == 1 && !dense) ? (ti.valid + 3) / 4 : 0;
-            const uint32_t a_tx = (MODE == 1) ? (dense ? (dense_small ? (uint32_t)kDenseBoxRows * BK : (uint32_t)A_STAGE)
-                                                       : (uint32_t)a_gathers * 4 * BK)
+            const uint32_t a_tx = (MODE == 1) ? (dense_big ? (uint32_t)A_STAGE
+                                                 : dense ? (uint32_t)dense_boxes * kDenseBoxRows * BK
+                                                         : (uint32_t)a_gathers * 4 * BK)
                                               : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
             // A's scales change every fourth stage, and only those stages' copy is
             // read (the MMA thread moves it into tensor memory there)
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             // (once GEMM1 has finished altogether no tile needs to wait: the
             // first look at the total usually says so, costing one load per CTA)
             if (MODE == 2 && !gemm1_done) {
-                const int per_tile = (TR <= 32 ? 2 : EPI_WARPS) * (g.K / 128);
+                const int per_tile = C::EPI_Q * 2 * (g.K / 128);
                 // (test flag: a count GEMM1 never reaches, so the wait runs out
                 // before this CTA issues any copy)
                 if (lane == 0) {
@@ -308,7 +315,9 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 armed++;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, stage_tx + ((ks & 3) == 0 ? SFA_STAGE : 0));
-                    if (dense) tma_load_2d(sa, dense_small ? &tmA3 : &tmA2, fb, ks * BK, ti.row0);
+                    if (dense_big) tma_load_2d(sa, &tmA2, fb, ks * BK, ti.row0);
+                    for (int b = 0; b < dense_boxes; b++)
+                        tma_load_2d(sa + b * kDenseBoxRows * BK, &tmA3, fb, ks * BK, ti.row0 + b * kDenseBoxRows);
                     if (MODE == 2) {
                         if (small) {
                             for (int b = 0; b < a_boxes; b++)
@@ -457,8 +466,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
         const int r = q * 32 + lane;               // accumulator row = pair row in the tile
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL;
         uint32_t acc_phase = 0, tpar = 0;
-        // 16- and 32-row tiles have no rows in lane quarters 1-3
-        for (long long tile = blockIdx.x; (TR == 128 || q == 0) && tile < total_tiles && !*abort_flag;
+        // small tiles have no rows in the lane quarters from EPI_Q on
+        for (long long tile = blockIdx.x; q < C::EPI_Q && tile < total_tiles && !*abort_flag;
              tile += gridDim.x) {
             const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb, TR);
             if (!mbar_wait(acc_full, acc_phase, tmo, abort_flag)) {
@@ -655,6 +664,12 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
         threads = gg::Cfg<32>::NUM_THREADS;
         if constexpr (MODE == 1)
             if (dense) kern = gg::grouped_gemm_kernel<1, true, 32>;
+    } else if (a.tile_rows == 64) {
+        kern = gg::grouped_gemm_kernel<MODE, false, 64>;
+        smem = gg::Cfg<64>::SMEM_BYTES;
+        threads = gg::Cfg<64>::NUM_THREADS;
+        if constexpr (MODE == 1)
+            if (dense) kern = gg::grouped_gemm_kernel<1, true, 64>;
     } else if (a.tile_rows == 128) {
         if constexpr (MODE == 1)
             if (dense) kern = gg::grouped_gemm_kernel<1, true, 128>;

@@ -243,6 +243,8 @@ def test_forward_tiny_all_tokens():
     (60, 256, 128, 8, 2, False),         # 32-row tiles, every A row gathered (under 16 pairs per expert)
     (76, 512, 256, 8, 2, True),          # 32-row tiles with the expert-ordered copy; biased: experts over 32 pairs
     (150, 256, 128, 16, 2, True),        # 32-row tiles with the copy, ragged tails and empty experts
+    (90, 512, 128, 8, 2, False),         # 64-row tiles: one or two 32-row boxes of the copy per stage
+    (120, 256, 256, 8, 2, True),         # 64-row tiles, biased: experts over 64 pairs, empty experts
 ])
 def test_forward_small_shapes(T, d, inter, E, k, bias):
     w, x, gw, b, w13, w2 = small_case(T, d, inter, E, k, seed=T + d, bias=bias)
@@ -316,7 +318,7 @@ def _workload(name, cache):
     return cache[name]
 
 
-@pytest.mark.parametrize("name", ["decode", "decode384", "decode512", "mid", "skew", "prefill"])
+@pytest.mark.parametrize("name", ["decode", "decode384", "decode512", "decode1024", "mid", "skew", "prefill"])
 def test_forward_full_size_sampled_tokens(name, workload_cache):
     """Full-size workloads in the benchmark's launch configuration; the oracle
     recomputes a seeded sample of tokens (every token is independent)."""
@@ -388,7 +390,7 @@ def test_workspace_intermediates_tiny():
     f2, s2 = oracle.pack_fp4(w2.numpy())
     hq = wsn[off[c.MOE_WS_HQ]:][:w.P * w.inter].reshape(w.P, w.inter)
     tp = wsn[off[c.MOE_WS_TILE_PREFIX]:][:4 * (w.E + 1)].view(np.int32)
-    R = 16 if w.P <= 8 * w.E else 32 if w.P <= 20 * w.E else 128    # pair rows per GEMM row tile
+    R = 16 if w.P <= 8 * w.E else 32 if w.P <= 20 * w.E else 64 if w.P <= 40 * w.E else 128    # rows per tile
     assert np.array_equal(tp, np.concatenate([[0], np.cumsum((np.diff(offs) + R - 1) // R)]))
     hs_tiles = wsn[off[c.MOE_WS_HS_TILES]:]
     GH = (w.inter // 128 + 3) // 4
