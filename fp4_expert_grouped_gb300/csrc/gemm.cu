@@ -15,7 +15,8 @@
 // blocks are shared through L2, and the TMA loads of the next tiles run while
 // the current tile's MMAs execute.
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads; 352 with the scale-factor warp of 16-, 32- and
+// 64-row tiles):
 //   warp 0      producer: GEMM1 gathers the tile's token rows of A (E4M3)
 //               with four-row TMA gathers (the dispatch to expert order
 //               happens here);
@@ -58,14 +59,14 @@ constexpr int SF_WARP = 2 + EPI_WARPS;    // B scale-factor copies into tensor m
 // Shared-memory layout per tile size TR (pair rows per tile).  TR = 128: a
 // 4-stage ring of 48 KB stages (A 16 KB, B 32 KB).  TR = 16: A slots of 2 KB
 // and a 6-stage ring (50% more weight bytes in flight); TR = 32 and 64: 4 and
-// 8 KB slots, 5 stages (a sixth does not fit).  The MMA always reads 128 A rows (16 KB)
-// from a slot's start; with smaller slots the rows past TR come from whatever
-// follows the slot in shared memory and only feed accumulator rows that are
-// discarded.  The A slots therefore come first.
+// 8 KB slots, 5 stages (a sixth does not fit).  The MMA always reads 128 A
+// rows (16 KB) from a slot's start; with smaller slots the rows past TR come
+// from whatever follows the slot in shared memory and only feed accumulator
+// rows that are discarded.  The A slots therefore come first.
 template <int TR>
 struct Cfg {
     static constexpr int STAGES = TR == 16 ? 6 : TR <= 64 ? 5 : 4;
-    // 16/32-row tiles stream weights through a deep ring: a separate warp copies
+    // 16/32/64-row tiles stream weights through a deep ring: a separate warp copies
     // B's scale factors into tensor memory, keeping the MMA thread's per-stage
     // issue work under the stage's MMA time (decode GEMM1 363 -> 352 us).  With
     // 128-row tiles and a 4-deep ring the extra hop's latency cost more (large
