@@ -242,7 +242,7 @@ enum {
     MOE_WS_SORTED_PAIR,   /* int32 [P] */
     MOE_WS_PAIR_POS,      /* int32 [P] */
     MOE_WS_TILE_PREFIX,   /* int32 [E+1] running count of the GEMMs' row tiles of R pairs each:
-                             R = 16 when T*k <= 8*E, 32 when <= 20*E, 64 when <= 40*E, else 128 */
+                             R = 16 when T*k <= 8*E, 32 when <= 20*E, 64 when <= 48*E, else 128 */
     MOE_WS_HQ,            /* uint8 E4M3 [P][inter], rows in expert order */
     MOE_WS_HS_TILES,      /* uint8 scales of hq per row tile m (R rows, as above) and
                              group g of four 128-channel groups: 512-byte blocks

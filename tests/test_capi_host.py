@@ -104,7 +104,7 @@ def test_workspace_layout(capi):
         assert total == capi.moe_workspace_size(T, d, inter, E, k) > 0
         P = T * k
         xs = ((d // 128) + 3) // 4 * 4
-        R = 16 if P <= 8 * E else 32 if P <= 20 * E else 64 if P <= 40 * E else 128    # rows per GEMM row tile
+        R = 16 if P <= 8 * E else 32 if P <= 20 * E else 64 if P <= 48 * E else 128    # rows per GEMM row tile
         tiles = (P + R - 1) // R + min(P, E)
         gx, gh = (d // 128 + 3) // 4, (inter // 128 + 3) // 4
         chunks = (P + 2047) // 2048

@@ -390,7 +390,7 @@ def test_workspace_intermediates_tiny():
     f2, s2 = oracle.pack_fp4(w2.numpy())
     hq = wsn[off[c.MOE_WS_HQ]:][:w.P * w.inter].reshape(w.P, w.inter)
     tp = wsn[off[c.MOE_WS_TILE_PREFIX]:][:4 * (w.E + 1)].view(np.int32)
-    R = 16 if w.P <= 8 * w.E else 32 if w.P <= 20 * w.E else 64 if w.P <= 40 * w.E else 128    # rows per tile
+    R = 16 if w.P <= 8 * w.E else 32 if w.P <= 20 * w.E else 64 if w.P <= 48 * w.E else 128    # rows per tile
     assert np.array_equal(tp, np.concatenate([[0], np.cumsum((np.diff(offs) + R - 1) // R)]))
     hs_tiles = wsn[off[c.MOE_WS_HS_TILES]:]
     GH = (w.inter // 128 + 3) // 4
