@@ -66,15 +66,14 @@ inline int scale_row_stride(int channels) { return ((channels / 128) + 3) / 4 * 
 
 // upper bound on the number of 128-row tiles of the expert-ordered pairs
 // Pair rows per GEMM row tile: 16 for batches averaging at most 8 pairs per
-// expert, 32 up to 20, 64 up to 48 (an expert's pair count is then above the
-// tile for about one expert in 200 (32-row tiles) or 75 (64-row) at the top
-// of each range, and that one
-// streams its weights twice), 128 otherwise.  A
-// small batch's tiles hold a few rows each, and the shared memory a 128-row A
-// slot takes is better spent on a deeper ring of weight stages (the GEMMs
-// then stream weights at ~90% of HBM bandwidth instead of ~80%).  The MMA
-// still computes 128 rows; rows past the tile's own are discarded, so a row's
-// result does not depend on the tile size.
+// expert, 32 up to 20, 64 up to 48, 128 otherwise.  At the top of each range
+// about one expert in 200 (32-row tiles) or 75 (64-row tiles) holds more
+// pairs than a tile and streams its weights twice.  A small batch's tiles
+// hold a few rows each, and the shared memory a 128-row A slot takes is
+// better spent on a deeper ring of weight stages (the GEMMs then stream
+// weights at ~90% of HBM bandwidth instead of ~80%).  The MMA still computes
+// 128 rows; rows past the tile's own are discarded, so a row's result does
+// not depend on the tile size.
 __host__ __device__ inline int gemm_tile_rows(long long P, int E)
 {
     return P <= 8LL * E ? 16 : P <= 20LL * E ? 32 : P <= 48LL * E ? 64 : kTileM;
