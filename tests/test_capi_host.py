@@ -99,7 +99,9 @@ def test_other_entry_points_reject_bad_arguments(capi):
 
 
 def test_workspace_layout(capi):
-    for (T, d, inter, E, k) in [(32, 256, 128, 8, 2), (128, 4096, 2048, 256, 8), (16384, 7168, 2048, 256, 8)]:
+    # row tiles of 16 (the first two), 32, 64 and 128 pairs
+    for (T, d, inter, E, k) in [(32, 256, 128, 8, 2), (128, 4096, 2048, 256, 8), (512, 4096, 2048, 256, 8),
+                                (1536, 4096, 2048, 256, 8), (16384, 7168, 2048, 256, 8)]:
         total, off, st = capi.moe_workspace_layout(T, d, inter, E, k)
         assert total == capi.moe_workspace_size(T, d, inter, E, k) > 0
         P = T * k
