@@ -53,6 +53,8 @@ def lib():
         L.orc_quant_act.restype = None
         L.orc_pack_fp4.argtypes = [f32p, c_int, c_int, c_int, u8p, u8p]
         L.orc_pack_fp4.restype = None
+        L.orc_fp4_to_fp8t.argtypes = [u8p, u8p, c_int, c_int, c_int, u8p, u8p]
+        L.orc_fp4_to_fp8t.restype = None
         L.orc_gate_logits.argtypes = [u16p, f32p, f32p, c_int, c_int, c_int, f32p]
         L.orc_gate_logits.restype = None
         L.orc_topk.argtypes = [f32p, c_int, c_int, c_int, i32p, f32p]
@@ -145,6 +147,22 @@ def pack_fp4(w):
     w_scale = np.empty((E, N, K // 32), np.uint8)
     lib().orc_pack_fp4(_p(w, ctypes.c_float), E, N, K, _p(w_fp4, ctypes.c_uint8), _p(w_scale, ctypes.c_uint8))
     return w_fp4, w_scale
+
+
+def fp4_to_fp8t(w_fp4, w_scale):
+    """FP8 weights for the backward pass, transposed: (w8t uint8 [E, K, N]
+    E4M3 codes, s8t uint8 [E, K/128, N/128] UE8M0 block exponents + 127)."""
+    w_fp4 = _c(w_fp4, np.uint8)
+    w_scale = _c(w_scale, np.uint8)
+    if w_fp4.ndim == 2:
+        w_fp4, w_scale = w_fp4[None], w_scale[None]
+    E, N, K2 = w_fp4.shape
+    K = 2 * K2
+    w8t = np.empty((E, K, N), np.uint8)
+    s8t = np.empty((E, K // 128, N // 128), np.uint8)
+    lib().orc_fp4_to_fp8t(_p(w_fp4, ctypes.c_uint8), _p(w_scale, ctypes.c_uint8), E, N, K,
+                          _p(w8t, ctypes.c_uint8), _p(s8t, ctypes.c_uint8))
+    return w8t, s8t
 
 
 def gate_logits(x, gate_w, bias=None):

@@ -225,6 +225,46 @@ void orc_pack_fp4(const float *w, int E, int N, int K, uint8_t *w_fp4, uint8_t *
     }
 }
 
+/* FP8 weights for the backward pass ("DeepSeek-V4揭秘…" section 4, FP4 QAT:
+ * the FP4 weights are dequantised to FP8 for compute, losslessly while the
+ * 1x32 sub-block scales of each 128x128 FP8 block stay within a ratio; the
+ * backward uses these FP8 weights, and 128x128 blocks transpose without
+ * re-quantisation).
+ * For each 128x128 block of W[e] ([N][K]): S = the largest sub-block
+ * exponent X in the block, the block exponent B = S - 6 clamped to >= -127
+ * [R]; each element becomes E4M3_RNE(code_value * 2^(X - B)), exact whenever
+ * X - B >= -8.  Output transposed: w8t [E][K][N] E4M3 codes, s8t
+ * [E][K/128][N/128] UE8M0 bytes B + 127.  Input in the row-major layout of
+ * orc_pack_fp4.  N % 128 == 0, K % 128 == 0. */
+void orc_fp4_to_fp8t(const uint8_t *w_fp4, const uint8_t *w_scale, int E, int N, int K, uint8_t *w8t,
+                     uint8_t *s8t)
+{
+    const int NB = N / 128, KB = K / 128;
+#pragma omp parallel for schedule(static)
+    for (long blk = 0; blk < (long)E * NB * KB; blk++) {
+        const int e = (int)(blk / ((long)NB * KB));
+        const int bn = (int)((blk / KB) % NB);
+        const int bk = (int)(blk % KB);
+        int S = -127;
+        for (int n = bn * 128; n < bn * 128 + 128; n++)
+            for (int j = bk * 4; j < bk * 4 + 4; j++) {
+                int X = (int)w_scale[((long)e * N + n) * (K / 32) + j] - 127;
+                if (X > S) S = X;
+            }
+        int B = S - 6;
+        if (B < -127) B = -127;
+        s8t[((long)e * KB + bk) * NB + bn] = (uint8_t)(B + 127);
+        for (int n = bn * 128; n < bn * 128 + 128; n++)
+            for (int k = bk * 128; k < bk * 128 + 128; k++) {
+                const long row = (long)e * N + n;
+                const uint8_t byte = w_fp4[row * (K / 2) + k / 2];
+                const uint8_t code = (k & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+                const int X = (int)w_scale[row * (K / 32) + k / 32] - 127;
+                w8t[((long)e * K + k) * N + n] = orc_e4m3_encode(ldexp(orc_e2m1_decode(code), X - B));
+            }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Gate                                                                     */
 /* ------------------------------------------------------------------------ */

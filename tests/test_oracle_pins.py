@@ -509,3 +509,54 @@ def test_expert_pair_intermediates():
     assert np.array_equal(t_e4m3_encode(np.ldexp(h.astype(np.float64), -np.repeat(e[0], 128)).astype(np.float32)), hq)
     yref = bf16_bits_of((np_dequant_fp4(w2f, w2s)[1] @ hd[0]).astype(np.float32))
     assert np.max(np.abs(from_bits(y) - from_bits(yref))) <= 2.0 ** -7 * np.abs(from_bits(yref)).max()
+
+
+# --------------------------------------------------------------------------
+# FP8 weights for the backward pass (FP4 QAT, "DeepSeek-V4揭秘…" section 4)
+# --------------------------------------------------------------------------
+
+def np_block_exponents(w_scale):
+    """B = max(largest 1x32 exponent of each 128x128 block - 6, -127), as [E, K/128, N/128]."""
+    E, N, KS = w_scale.shape
+    X = w_scale.astype(np.int64).reshape(E, N // 128, 128, KS // 4, 4) - 127
+    S = X.max(axis=(2, 4))                                   # [E, N/128, K/128]
+    return np.maximum(S - 6, -127).transpose(0, 2, 1)
+
+
+def test_fp8t_is_lossless_on_weights_within_the_scale_ratio():
+    """The pages' claim: while each 128x128 block's sub-block scales stay within
+    a 2^14 ratio, the FP8 weights are the FP4 weights exactly (here: transposed)."""
+    rng = np.random.default_rng(11)
+    E, N, K = 3, 256, 384
+    w = (rng.normal(0, 1, (E, N, K)) / np.sqrt(K)).astype(np.float32)
+    w[1, 128:, :128] = 0.0                                   # an all-zero block
+    f, s = oracle.pack_fp4(w)
+    w8t, s8t = oracle.fp4_to_fp8t(f, s)
+    B = np_block_exponents(s)
+    assert np.array_equal(s8t.astype(np.int64) - 127, B)
+    X = s.astype(np.int64).reshape(E, N // 128, 128, K // 128, 4) - 127
+    spread = X.max(axis=(2, 4)) - np.where(X.min(axis=(2, 4)) < -120, X.max(axis=(2, 4)), X.min(axis=(2, 4)))
+    assert spread.max() <= 14
+    got = t_e4m3_decode(w8t) * np.ldexp(1.0, np.repeat(np.repeat(B, 128, 1), 128, 2))
+    assert np.array_equal(got, np_dequant_fp4(f, s).transpose(0, 2, 1))
+    assert np.all(w8t[1, :128, 128:] == 0) and s8t[1, 0, 1] == 0   # zero block: B clamped to -127
+
+
+def test_fp8t_rounds_sub_blocks_beyond_the_ratio():
+    """A block whose sub-scales span more than 2^14: the large sub-block stays
+    exact, the small one is rounded to nearest-even E4M3 at the block's scale."""
+    rng = np.random.default_rng(12)
+    w = np.zeros((1, 128, 128), np.float32)
+    w[0, :, :32] = rng.uniform(-300, 300, (128, 32))          # exponents near 6
+    w[0, :, 32:64] = rng.uniform(-1, 1, (128, 32)) * 2.0 ** -16   # about 2^22 smaller
+    f, s = oracle.pack_fp4(w)
+    w8t, s8t = oracle.fp4_to_fp8t(f, s)
+    B = int(s8t[0, 0, 0]) - 127
+    deq = np_dequant_fp4(f, s)[0]                             # [N, K]
+    X = s[0].astype(np.int64) - 127
+    assert X[:, 0].max() - X[:, 1].max() > 14
+    want = t_e4m3_encode(np.ldexp(deq, -B).astype(np.float32)).T   # exact in fp32: codes times powers of two
+    assert np.array_equal(w8t[0], want)
+    big = t_e4m3_decode(w8t[0, :32, :]) * 2.0 ** B
+    assert np.array_equal(big, deq[:, :32].T)
+    assert not np.array_equal(t_e4m3_decode(w8t[0, 32:64, :]) * 2.0 ** B, deq[:, 32:64].T)
