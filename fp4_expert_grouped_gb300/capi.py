@@ -30,7 +30,7 @@ STAGES = ["gate", "topk", "plan", "dispatch", "gemm1", "gemm2", "combine"]
  MOE_WS_XQ_SORTED, MOE_WS_XS_TILES, MOE_WS_PLAN_COUNTS, MOE_WS_TILE_DONE, MOE_WS_COUNT) = range(17)
 
 # every symbol the header declares
-EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_quantize_act", "moe_route",
+EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_fp4_to_fp8t", "moe_quantize_act", "moe_route",
            "moe_route_noalloc", "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
            "moe_workspace_layout", "moe_get_device_status"]
 
@@ -49,6 +49,8 @@ _lib.moe_version.argtypes = []
 _lib.moe_version.restype = _i
 _lib.moe_pack_fp4.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp]
 _lib.moe_pack_fp4.restype = _i
+_lib.moe_fp4_to_fp8t.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]
+_lib.moe_fp4_to_fp8t.restype = _i
 _lib.moe_quantize_act.argtypes = [_vp, _vp, _vp, _i, _i, _vp]
 _lib.moe_quantize_act.restype = _i
 _lib.moe_route.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
@@ -114,6 +116,14 @@ def moe_pack_fp4(w, w_fp4, w_scale, stream=None):
     device tensors of any shape with that many bytes (see include/fp4moe.h)."""
     E, N, K = w.shape if w.dim() == 3 else (1, *w.shape)
     _check(_lib.moe_pack_fp4(_ptr(w), _ptr(w_fp4), _ptr(w_scale), E, N, K, _stream(stream)), "moe_pack_fp4")
+
+
+def moe_fp4_to_fp8t(w_fp4, w_scale, w8t, s8t, stream=None):
+    """w_fp4 uint8 [E, N, K/2], w_scale [E, N, K/32] (moe_pack_fp4 output) ->
+    w8t uint8 [E, K, N] E4M3 codes, s8t uint8 [E, K/128, N/128] block exponents + 127."""
+    E, N, K2 = w_fp4.shape
+    _check(_lib.moe_fp4_to_fp8t(_ptr(w_fp4), _ptr(w_scale), _ptr(w8t), _ptr(s8t), E, N, 2 * K2, _stream(stream)),
+           "moe_fp4_to_fp8t")
 
 
 def moe_quantize_act(x, xq, xs, stream=None):

@@ -166,6 +166,21 @@ moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E,
     return cuda_status(launch_pack_fp4(w, w_fp4, w_scale, E, N, K, (cudaStream_t)stream));
 }
 
+moe_status moe_fp4_to_fp8t(const uint8_t *w_fp4, const uint8_t *w_scale, uint8_t *w8t, uint8_t *s8t, int E, int N,
+                           int K, void *stream)
+{
+    if (!w_fp4 || !w_scale || !w8t || !s8t) return MOE_ERR_INVALID_ARG;
+    if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w_fp4, 16) || !aligned(w_scale, 16) || !aligned(w8t, 16)) return MOE_ERR_INVALID_ARG;
+    if (K % 128 || N % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)E * N * K == 0) return MOE_OK;
+    if ((long long)E * (N / 128) * (K / 128) > 0x7FFFFFFFLL) return MOE_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo *di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return cuda_status(launch_fp4_to_fp8t(w_fp4, w_scale, w8t, s8t, E, N, K, (cudaStream_t)stream));
+}
+
 moe_status moe_quantize_act(const uint16_t *x, uint8_t *xq, uint8_t *xs, int T, int d, void *stream)
 {
     if (!x || !xq || !xs) return MOE_ERR_INVALID_ARG;

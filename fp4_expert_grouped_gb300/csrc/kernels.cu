@@ -77,6 +77,106 @@ cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, in
 }
 
 // ---------------------------------------------------------------------------
+// FP8 weights for the backward pass (FP4 QAT): every 128 x 128 block of the
+// packed weights becomes E4M3 codes at one power-of-two block scale B (the
+// block's largest 1x32 exponent - 6, at least -127), written transposed.
+// One CTA per block: the scales' maximum, the codes staged in shared memory,
+// then warp w writes the 16 codes of rows n = 16w .. 16w+15 of every output
+// row k as a 16-byte vector (lane = k % 32: the lanes read a shared 16-byte
+// span of one code row, so the reads broadcast).  code * 2^(X - B) is exact in fp32 down to its subnormals (it is
+// below E4M3's half-ulp, so rounds to a signed zero, whenever it is smaller),
+// and the E4M3 conversion rounds to nearest even.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float e2m1_value(uint32_t code)
+{
+    const uint32_t e = (code >> 1) & 3u, m = code & 1u;
+    const uint32_t mag = e ? ((e + 126u) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
+    return __uint_as_float(mag | ((code & 8u) << 28));
+}
+
+// 2^e as fp32 for any e (subnormal, or zero below 2^-149)
+__device__ __forceinline__ float pow2_any(int e)
+{
+    if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+    if (e >= -149) return __uint_as_float(1u << (e + 149));
+    return 0.f;
+}
+
+constexpr int kF8tRow = 64;                   // shared-memory row of 128 codes
+
+__global__ void __launch_bounds__(256) fp4_to_fp8t_kernel(const uint8_t *__restrict__ w_fp4,
+                                                          const uint8_t *__restrict__ w_scale,
+                                                          uint8_t *__restrict__ w8t, uint8_t *__restrict__ s8t,
+                                                          int N, int K)
+{
+    pdl_wait();
+    __shared__ __align__(16) uint8_t codes[128 * kF8tRow];
+    __shared__ __align__(16) uint8_t sc[kBlockScaleBytes];
+    __shared__ int s_max[8];
+    const int NB = N / 128, KB = K / 128;
+    const int bk = blockIdx.x % KB, bn = (blockIdx.x / KB) % NB, e = blockIdx.x / (KB * NB);
+    const long long blk = weight_block(e, bn, bk, N, K);
+    const uint8_t *src = w_fp4 + blk * kBlockCodeBytes;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    // codes: 8 KB, 32 bytes per thread, into rows of kF8tRow bytes
+    {
+        const int r = t >> 1, half = t & 1;
+        const uint4 *g = reinterpret_cast<const uint4 *>(src + r * 64 + half * 32);
+        uint4 *d = reinterpret_cast<uint4 *>(codes + r * kF8tRow + half * 32);
+        d[0] = __ldg(g);
+        d[1] = __ldg(g + 1);
+    }
+    int m = -127;
+    {
+        const uint16_t two = __ldg(reinterpret_cast<const uint16_t *>(w_scale + blk * kBlockScaleBytes) + t);
+        reinterpret_cast<uint16_t *>(sc)[t] = two;
+        m = max((int)(two & 0xFF), (int)(two >> 8)) - 127;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) s_max[warp] = m;
+    __syncthreads();
+    int S = s_max[0];
+#pragma unroll
+    for (int w = 1; w < 8; w++) S = max(S, s_max[w]);
+    const int B = max(S - 6, -127);
+    if (t == 0) s8t[((long long)e * KB + bk) * NB + bn] = (uint8_t)(B + 127);
+    // output rows k of the block, 16 codes (16 rows n) per lane
+    const int n0 = warp * 16;
+    for (int k = lane; k < 128; k += 32) {
+        const int j = k >> 5;                     // 32-element sub-block of K
+        uint32_t out[4];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            float v2[2];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int n = n0 + 2 * u + h;
+                const uint32_t byte = codes[n * kF8tRow + (k >> 1)];
+                const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
+                const int X = (int)sc[sf_byte(n, j)] - 127;
+                v2[h] = e2m1_value(code) * pow2_any(X - B);
+            }
+            const uint32_t c2 = cvt_e4m3x2(v2[0], v2[1]);
+            if (u & 1) out[u >> 1] |= c2 << 16;
+            else out[u >> 1] = c2;
+        }
+        uint8_t *dst = w8t + ((long long)e * K + (long long)bk * 128 + k) * N + (long long)bn * 128 + n0;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_fp4_to_fp8t(const uint8_t *w_fp4, const uint8_t *w_scale, uint8_t *w8t, uint8_t *s8t, int E, int N,
+                               int K, cudaStream_t st)
+{
+    const long long blocks = (long long)E * (N / 128) * (K / 128);
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    return launch_pdl(fp4_to_fp8t_kernel, dim3((unsigned)blocks), dim3(256), 0, st, w_fp4, w_scale, w8t, s8t, N, K);
+}
+
+// ---------------------------------------------------------------------------
 // FP8 quantisation of one 128-channel group of a bf16 row by one warp:
 // each lane handles 4 channels; returns the group's scale exponent e.
 // ---------------------------------------------------------------------------

@@ -109,6 +109,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // ---- launchers (kernels.cu) ----------------------------------------------
 // rows = E * N; writes the tiled layout above (N % 256 == 0, K % 128 == 0)
 cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E, int N, int K, cudaStream_t st);
+// FP8 weights for the backward pass, transposed (N % 256 == 0, K % 128 == 0):
+// w8t [E][K][N] E4M3 codes, s8t [E][K/128][N/128] block exponents + 127
+cudaError_t launch_fp4_to_fp8t(const uint8_t *w_fp4, const uint8_t *w_scale, uint8_t *w8t, uint8_t *s8t, int E, int N,
+                               int K, cudaStream_t st);
 cudaError_t launch_quantize(const uint16_t *x, uint8_t *xq, uint8_t *xs, int xs_stride, int T, int d,
                             cudaStream_t st);
 cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const float *bias, float *z, int T, int d,

@@ -94,6 +94,28 @@ moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale,
                         int E, int N, int K, void *stream);
 
 /*
+ * moe_fp4_to_fp8t -- FP8 weights for the backward pass of FP4 quantisation-
+ * aware training (first page, section 4: the FP4 weights are dequantised to
+ * FP8 for compute, losslessly while the 1x32 sub-block scales inside each
+ * 128x128 FP8 block stay within a ratio; gradients use these FP8 weights, and
+ * 128x128 blocks transpose without re-quantisation).  For every 128x128 block
+ * of W[e] ([N][K]): block exponent B = (largest 1x32 exponent X of the block)
+ * - 6, clamped to >= -127; each element is E4M3(code * 2^(X - B)) rounded to
+ * nearest even -- exactly the FP4 value over 2^B when X - B >= -8, i.e. when
+ * the block's sub-block scales span at most 2^14.
+ *   w_fp4, w_scale  device, moe_pack_fp4 output (tiled layout) of W [E][N][K]
+ *   w8t             device, E*K*N bytes: E4M3 code of W[e][n][k] at
+ *                   (e * K + k) * N + n (transposed, N contiguous), 16-byte aligned
+ *   s8t             device, E*(K/128)*(N/128) bytes: B + 127 of block (bn, bk)
+ *                   at (e * K/128 + bk) * N/128 + bn
+ * Requires N % 256 == 0, K % 128 == 0.  Argument errors are reported before
+ * any launch; the outputs are written on the stream.  Load-time operation
+ * (once per weight update), off the forward's hot path.
+ */
+moe_status moe_fp4_to_fp8t(const uint8_t *w_fp4, const uint8_t *w_scale, uint8_t *w8t, uint8_t *s8t,
+                           int E, int N, int K, void *stream);
+
+/*
  * moe_quantize_act -- FP8 E4M3 activation quantisation (first page, section 1.4,
  * "FP8 dispatch").  One power-of-two scale per token per 128 channels:
  * e = the smallest integer with max|x| <= 448 * 2^e (e = 0 for an all-zero

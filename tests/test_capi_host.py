@@ -98,6 +98,16 @@ def test_other_entry_points_reject_bad_arguments(capi):
     assert lib.moe_dispatch_plan(FAKE, FAKE, FAKE, FAKE, 4, 300, 2, None) == 2
 
 
+def test_fp4_to_fp8t_argument_checks(capi):
+    lib = capi._lib
+    assert lib.moe_fp4_to_fp8t(None, FAKE, FAKE, FAKE, 1, 256, 128, None) == 1
+    assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE + 8, FAKE, 1, 256, 128, None) == 1     # w8t not 16-byte aligned
+    assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, -1, 256, 128, None) == 1
+    assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, 1, 128, 128, None) == 2          # N % 256
+    assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, 1, 256, 96, None) == 2           # K % 128
+    assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, 0, 256, 128, None) == 0          # nothing to do
+
+
 def test_workspace_layout(capi):
     # row tiles of 16 (the first two), 32, 64 and 128 pairs
     for (T, d, inter, E, k) in [(32, 256, 128, 8, 2), (128, 4096, 2048, 256, 8), (512, 4096, 2048, 256, 8),

@@ -108,3 +108,33 @@ def test_e4m3_conversion_exhaustive_over_bf16():
     full = np.zeros(-(-p.size // d) * d, np.uint16)
     full[:p.size] = p
     _quantize(full.reshape(-1, d))
+
+
+@pytest.mark.parametrize("E,N,K", [(3, 512, 384), (1, 256, 128)])
+def test_fp4_to_fp8t_bitexact(E, N, K):
+    """FP8 weights for the backward pass (transposed, one exponent per 128x128
+    block) from the GPU pack: the oracle's codes and block exponents bit for bit,
+    on trained-like weights, an all-zero block and a block whose sub-block
+    scales span more than 2^14 (rounded, not lossless)."""
+    c = capi()
+    rng = np.random.default_rng(E * N + K)
+    w = (rng.normal(0, 1, (E, N, K)) / np.sqrt(K)).astype(np.float32)
+    w[0, :128, :128] = 0.0
+    if E > 1:
+        w[E - 1, 128:256, 128:160] = rng.uniform(-300, 300, (128, 32))
+        w[E - 1, 128:256, 160:192] = rng.uniform(-1, 1, (128, 32)) * 2.0 ** -16
+    wd = torch.from_numpy(w).to(DEV)
+    fp4 = torch.empty((E, N, K // 2), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((E, N, K // 32), dtype=torch.uint8, device=DEV)
+    c.moe_pack_fp4(wd, fp4, sc)
+    w8t = torch.empty((E, K, N), dtype=torch.uint8, device=DEV)
+    s8t = torch.empty((E, K // 128, N // 128), dtype=torch.uint8, device=DEV)
+    c.moe_fp4_to_fp8t(fp4, sc, w8t, s8t)
+    of, os_ = oracle.pack_fp4(w)
+    rw, rs = oracle.fp4_to_fp8t(of, os_)
+    assert np.array_equal(s8t.cpu().numpy(), rs)
+    got = w8t.cpu().numpy()
+    if not np.array_equal(got, rw):
+        bad = np.argwhere(got != rw)[:4]
+        pytest.fail("codes differ at (e, k, n) %s" % bad.tolist())
+    assert c.moe_get_device_status() == 0
