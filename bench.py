@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8t", action="store_true",
+                    help="instead of the layer: time moe_fp4_to_fp8t (FP8 weights for the backward pass) on "
+                         "the workload's W13 and W2 shapes and print one JSON line per matrix")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (a smaller case of the workload, e.g. for an ncu capture)")
     ap.add_argument("--experts", type=int, default=None,
@@ -461,6 +464,46 @@ def run_ours(args, w, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_fp8t(args, w):
+    """Device time of the FP8 backward-weight conversion on the workload's
+    packed W13 and W2 shapes (random packed bytes: the work does not depend on
+    them), against the measured HBM bandwidth."""
+    import torch
+    from fp4_expert_grouped_gb300 import capi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_gbs, _, _, peak_src = measured_peaks()
+    for name, N, K in (("W13", 2 * w.inter, w.d), ("W2", w.d, w.inter)):
+        g = torch.Generator(device=dev).manual_seed(0)
+        fp4 = torch.randint(0, 256, (w.E, N, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        sc = torch.randint(110, 135, (w.E, N, K // 32), dtype=torch.uint8, device=dev, generator=g)
+        w8t = torch.empty((w.E, K, N), dtype=torch.uint8, device=dev)
+        s8t = torch.empty((w.E, K // 128, N // 128), dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup):
+            capi.moe_fp4_to_fp8t(fp4, sc, w8t, s8t)
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            capi.moe_fp4_to_fp8t(fp4, sc, w8t, s8t)
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        st = capi.moe_get_device_status()
+        if st != 0:
+            raise RuntimeError("device status: " + capi.moe_status_string(st))
+        t = statistics.median(ms)
+        byts = w.E * N * K // 2 + w.E * N * K // 32 + w.E * K * N + w.E * (K // 128) * (N // 128)
+        gbs = byts / t / 1e6
+        print(json.dumps({"metric": "moe_fp4_to_fp8t throughput", "matrix": name, "E": w.E, "N": N, "K": K,
+                          "ms": t, "bytes": byts, "value": gbs, "unit": "GB/s",
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s",
+                                       "peak_note": peak_src, "frac": gbs / hbm_gbs}}), flush=True)
+        del fp4, sc, w8t, s8t
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     from fp4_expert_grouped_gb300 import inputs
@@ -470,6 +513,9 @@ def main():
         T = args.tokens or w.T
         E = args.experts or w.E
         w = dataclasses.replace(w, name="%s[T=%d,E=%d]" % (w.name, T, E), T=T, E=E)
+    if args.fp8t:
+        run_fp8t(args, w)
+        return
     world, rank, local = dist_setup(want_nccl=(args.impl == "ours"))
     if args.impl == "reference":
         run_reference(args, w, world, rank)
