@@ -560,3 +560,82 @@ def test_fp8t_rounds_sub_blocks_beyond_the_ratio():
     big = t_e4m3_decode(w8t[0, :32, :]) * 2.0 ** B
     assert np.array_equal(big, deq[:, :32].T)
     assert not np.array_equal(t_e4m3_decode(w8t[0, 32:64, :]) * 2.0 ** B, deq[:, 32:64].T)
+
+
+# --------------------------------------------------------------------------
+# QAT backward step of the expert path (oracle/qat.py) against autograd
+# --------------------------------------------------------------------------
+
+class _QuantGrad(torch.autograd.Function):
+    """Identity whose backward quantises the incoming gradient to E4M3 per 128
+    channels (independent numpy/PyTorch statement of the activation rule)."""
+
+    @staticmethod
+    def forward(ctx, v):
+        return v.clone()
+
+    @staticmethod
+    def backward(ctx, g):
+        return torch.from_numpy(np_fp8_quant(g.detach().numpy())[0])
+
+
+def _ste(v, value):
+    """Forward value `value`, gradient of `v` (straight-through)."""
+    return v + (torch.as_tensor(value, dtype=torch.float64) - v).detach()
+
+
+@pytest.mark.parametrize("quantize_grads", [False, True])
+def test_qat_backward_matches_autograd(quantize_grads):
+    """The oracle's backward step equals PyTorch float64 autograd of the same
+    forward (straight-through quantisers, fixed routing; with quantize_grads,
+    the gradients at y and at [g; u] quantised to E4M3 per 128 channels)."""
+    from oracle import qat
+    rng = np.random.default_rng(21)
+    T, d, inter, E, k = 5, 256, 128, 4, 2
+    w13 = (rng.normal(0, 1, (E, 2 * inter, d)) / np.sqrt(d)).astype(np.float32)
+    w2 = (rng.normal(0, 1, (E, d, inter)) / np.sqrt(inter)).astype(np.float32)
+    f13, s13 = oracle.pack_fp4(w13)
+    f2, s2 = oracle.pack_fp4(w2)
+    W13 = np_dequant_fp4(f13, s13)
+    W2 = np_dequant_fp4(f2, s2)
+    assert np.array_equal(qat.fp8_weights(f13, s13), W13)     # lossless: the backward's weights are the forward's
+    assert np.array_equal(qat.fp8_weights(f2, s2), W2)
+    xb = bf16_bits_of(rng.normal(0, 1, (T, d)))
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    tw = np.array([[0.75, 0.25]] * T, np.float32)              # dy = w * dout exact in fp32
+    doutb = bf16_bits_of(rng.normal(0, 1, (T, d)))
+    dx, dw, dW13, dW2 = qat.qat_backward(xb, idx, tw, f13, s13, f2, s2, doutb, quantize_grads=quantize_grads)
+
+    xq, xs = oracle.quant_act(xb)
+    xdq = np_fp8_quant(from_bits(xb))[0]
+    Wt13 = torch.tensor(W13, requires_grad=True)
+    Wt2 = torch.tensor(W2, requires_grad=True)
+    xd = torch.tensor(xdq, requires_grad=True)
+    wt = torch.tensor(tw.astype(np.float64), requires_grad=True)
+    out = torch.zeros((T, d), dtype=torch.float64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            gu = Wt13[e] @ xd[t]
+            if quantize_grads:
+                gu = _QuantGrad.apply(gu)
+            gu = _ste(gu, gu.detach().float().double())
+            g, u = gu[:inter], gu[inter:]
+            h = torch.nn.functional.silu(g) * u
+            _, hq, hs, yb = oracle.expert_pair(xq[t], xs[t], e, f13, s13, f2, s2)
+            hd = _ste(h, t_e4m3_decode(hq) * np.ldexp(1.0, np.repeat(hs.astype(np.int64) - 127, 128)))
+            y = Wt2[e] @ hd
+            if quantize_grads:
+                y = _QuantGrad.apply(y)
+            y = _ste(y, from_bits(yb).astype(np.float64))
+            out[t] = out[t] + wt[t, j] * y
+    (out * torch.from_numpy(from_bits(doutb).astype(np.float64))).sum().backward()
+
+    def close(a, b):
+        return np.linalg.norm(a - b) <= 1e-10 * max(np.linalg.norm(b), 1e-300)
+
+    assert close(dx, xd.grad.numpy())
+    assert close(dw, wt.grad.numpy())
+    assert close(dW13, Wt13.grad.numpy())
+    assert close(dW2, Wt2.grad.numpy())
+    assert np.abs(dW13).max() > 0 and np.abs(dx).max() > 0
