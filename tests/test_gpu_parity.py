@@ -368,6 +368,20 @@ def test_determinism_and_batch_invariance(name, workload_cache):
     assert capi().moe_get_device_status() == 0
 
 
+def test_batch_invariance_across_row_tile_sizes():
+    """The same tokens inside batches whose GEMMs pick 16-, 32- (with the
+    expert-ordered copy), 64- and 128-row tiles give the same bits: the row
+    tile only decides which rows share a tile."""
+    d, inter, E, k = 256, 128, 8, 2
+    w, x, gw, b, w13, w2 = small_case(300, d, inter, E, k, seed=5)
+    pk = layer().pack_experts(w13.to(DEV), w2.to(DEV))
+    sizes = (20, 76, 150, 300)                 # pairs per expert 5, 19, 37.5, 75
+    outs = [layer().forward(x[:T].to(DEV), gw.to(DEV), pk, k) for T in sizes]
+    assert capi().moe_get_device_status() == 0
+    for T, o in zip(sizes[1:], outs[1:]):
+        assert torch.equal(o[:sizes[0]], outs[0]), T
+
+
 def test_workspace_intermediates_tiny():
     """xq/xs in the workspace bit-exact; h (dequantised hq) close to the oracle's."""
     w = inputs.WORKLOADS["tiny"]
