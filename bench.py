@@ -104,8 +104,23 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
 
 
+# How long the clock sampler watches the timed work: a short timed region
+# (decode: ~11 ms) ends between two samples, so the same steps keep running,
+# untimed, until the GPU has been under this load for about this long.
+CLOCK_WINDOW_S = 1.0
+
+
+def clock_window_steps(ms_per_step, timed_steps, window_s=CLOCK_WINDOW_S, cap=20000):
+    """Untimed steps to run after `timed_steps` steps of `ms_per_step` so that
+    the work lasts about `window_s` in all (at most `cap`)."""
+    done = timed_steps * ms_per_step / 1e3
+    if ms_per_step <= 0 or done >= window_s:
+        return 0
+    return min(cap, int(math.ceil((window_s - done) / (ms_per_step / 1e3))))
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -117,7 +132,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                                          "-i", str(self.index), "-lms", "200"],
+                                          "-i", str(self.index), "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -125,7 +140,7 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.06)              # the last sample under load, not a stretch of idle ones
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
@@ -343,8 +358,12 @@ def run_ours(args, w, world, rank, local):
         pairs[s][1].record(stream)
     torch.cuda.synchronize(dev)
     dist_barrier()
-    ck = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in pairs]
+    for _ in range(clock_window_steps(statistics.mean(step_ms), args.steps)):
+        flush.zero_()
+        step(None)
+    torch.cuda.synchronize(dev)
+    ck = clocks.stop()
     ms_local = statistics.mean(step_ms)
     ms = dist_max(ms_local, dev)
     value = world * w.T / (ms / 1e3)

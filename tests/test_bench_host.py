@@ -44,6 +44,14 @@ def test_kernels_per_step_follow_the_library_thresholds():
     assert bench.kernels_per_step(edge) == 6
 
 
+def test_clock_window_keeps_the_gpu_busy_for_the_sampler():
+    assert bench.clock_window_steps(0.555, 20) == 1782        # decode: 11 ms timed, ~1 s in all
+    assert bench.clock_window_steps(6.2, 20) == 142           # prefill
+    assert bench.clock_window_steps(60.0, 20) == 0            # already longer than the window
+    assert bench.clock_window_steps(0.001, 1) == 20000        # capped
+    assert bench.clock_window_steps(0.0, 5) == 0
+
+
 def test_weight_bytes_per_expert():
     assert bench.weight_bytes_per_expert(4096, 2048) == 13_369_344
     assert bench.weight_bytes_per_expert(7168, 2048) == 23_396_352
