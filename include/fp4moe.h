@@ -160,8 +160,12 @@ moe_status moe_route(const uint16_t *x, const float *gate_w, const float *gate_b
  * experts); larger shapes return MOE_ERR_WORKSPACE without launching.
  * The first call on a device looks up that array's device address (once per
  * device, with the device current); make that first call before any stream
- * capture.  All calls share the array: calls that overlap on the GPU (e.g.
- * on two streams at once) race and must be serialised by the caller.
+ * capture.  Where the CUDA driver loads a library's device code lazily (its
+ * default), that first call is also when the driver loads the code holding
+ * the array and so reserves its 4 MiB: make it at start-up, with the other
+ * allocations; every later call allocates nothing.  All calls share the
+ * array: calls that overlap on the GPU (e.g. on two streams at once) race and
+ * must be serialised by the caller.
  */
 moe_status moe_route_noalloc(const uint16_t *x, const float *gate_w, const float *gate_bias,
                              int32_t *topk_idx, float *topk_w, int T, int d, int E, int k, void *stream);

@@ -21,57 +21,81 @@ from . import build as _build
 _lib = None
 
 
+def _load(path):
+    L = ctypes.CDLL(path)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    c_int = ctypes.c_int
+    L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_bf16_to_f32.restype = ctypes.c_float
+    L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.orc_f32_to_bf16.restype = ctypes.c_uint16
+    L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+    L.orc_e4m3_decode.restype = ctypes.c_double
+    L.orc_e4m3_encode.argtypes = [ctypes.c_double]
+    L.orc_e4m3_encode.restype = ctypes.c_uint8
+    L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+    L.orc_e2m1_decode.restype = ctypes.c_double
+    L.orc_e2m1_encode.argtypes = [ctypes.c_double]
+    L.orc_e2m1_encode.restype = ctypes.c_uint8
+    L.orc_e4m3_scale_exp.argtypes = [ctypes.c_double]
+    L.orc_e4m3_scale_exp.restype = c_int
+    L.orc_mx_scale_exp.argtypes = [ctypes.c_double]
+    L.orc_mx_scale_exp.restype = c_int
+    L.orc_gate_score.argtypes = [ctypes.c_float]
+    L.orc_gate_score.restype = ctypes.c_float
+    L.orc_quant_act.argtypes = [u16p, c_int, c_int, u8p, u8p]
+    L.orc_quant_act.restype = None
+    L.orc_pack_fp4.argtypes = [f32p, c_int, c_int, c_int, u8p, u8p]
+    L.orc_pack_fp4.restype = None
+    L.orc_fp4_to_fp8t.argtypes = [u8p, u8p, c_int, c_int, c_int, u8p, u8p]
+    L.orc_fp4_to_fp8t.restype = None
+    L.orc_gate_logits.argtypes = [u16p, f32p, f32p, c_int, c_int, c_int, f32p]
+    L.orc_gate_logits.restype = None
+    L.orc_topk.argtypes = [f32p, c_int, c_int, c_int, i32p, f32p]
+    L.orc_topk.restype = c_int
+    L.orc_dispatch_plan.argtypes = [i32p, c_int, c_int, c_int, i32p, i32p, i32p]
+    L.orc_dispatch_plan.restype = c_int
+    L.orc_expert_pair.argtypes = [u8p, u8p, c_int, u8p, u8p, u8p, u8p, c_int, c_int,
+                                  ctypes.POINTER(ctypes.c_double), f32p, u8p, u8p, u16p]
+    L.orc_expert_pair.restype = None
+    L.orc_moe_forward.argtypes = [u16p, f32p, f32p, u8p, u8p, u8p, u8p,
+                                  c_int, c_int, c_int, c_int, c_int,
+                                  i32p, c_int, u16p, i32p, f32p]
+    L.orc_moe_forward.restype = c_int
+    L.orc_num_threads.argtypes = []
+    L.orc_num_threads.restype = c_int
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        u8p = ctypes.POINTER(ctypes.c_uint8)
-        u16p = ctypes.POINTER(ctypes.c_uint16)
-        i32p = ctypes.POINTER(ctypes.c_int32)
-        f32p = ctypes.POINTER(ctypes.c_float)
-        c_int = ctypes.c_int
-        L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
-        L.orc_bf16_to_f32.restype = ctypes.c_float
-        L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
-        L.orc_f32_to_bf16.restype = ctypes.c_uint16
-        L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
-        L.orc_e4m3_decode.restype = ctypes.c_double
-        L.orc_e4m3_encode.argtypes = [ctypes.c_double]
-        L.orc_e4m3_encode.restype = ctypes.c_uint8
-        L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
-        L.orc_e2m1_decode.restype = ctypes.c_double
-        L.orc_e2m1_encode.argtypes = [ctypes.c_double]
-        L.orc_e2m1_encode.restype = ctypes.c_uint8
-        L.orc_e4m3_scale_exp.argtypes = [ctypes.c_double]
-        L.orc_e4m3_scale_exp.restype = c_int
-        L.orc_mx_scale_exp.argtypes = [ctypes.c_double]
-        L.orc_mx_scale_exp.restype = c_int
-        L.orc_gate_score.argtypes = [ctypes.c_float]
-        L.orc_gate_score.restype = ctypes.c_float
-        L.orc_quant_act.argtypes = [u16p, c_int, c_int, u8p, u8p]
-        L.orc_quant_act.restype = None
-        L.orc_pack_fp4.argtypes = [f32p, c_int, c_int, c_int, u8p, u8p]
-        L.orc_pack_fp4.restype = None
-        L.orc_fp4_to_fp8t.argtypes = [u8p, u8p, c_int, c_int, c_int, u8p, u8p]
-        L.orc_fp4_to_fp8t.restype = None
-        L.orc_gate_logits.argtypes = [u16p, f32p, f32p, c_int, c_int, c_int, f32p]
-        L.orc_gate_logits.restype = None
-        L.orc_topk.argtypes = [f32p, c_int, c_int, c_int, i32p, f32p]
-        L.orc_topk.restype = c_int
-        L.orc_dispatch_plan.argtypes = [i32p, c_int, c_int, c_int, i32p, i32p, i32p]
-        L.orc_dispatch_plan.restype = c_int
-        L.orc_expert_pair.argtypes = [u8p, u8p, c_int, u8p, u8p, u8p, u8p, c_int, c_int,
-                                      ctypes.POINTER(ctypes.c_double), f32p, u8p, u8p, u16p]
-        L.orc_expert_pair.restype = None
-        L.orc_moe_forward.argtypes = [u16p, f32p, f32p, u8p, u8p, u8p, u8p,
-                                      c_int, c_int, c_int, c_int, c_int,
-                                      i32p, c_int, u16p, i32p, f32p]
-        L.orc_moe_forward.restype = c_int
-        L.orc_num_threads.argtypes = []
-        L.orc_num_threads.restype = c_int
-        _lib = L
+        _lib = _load(_build.build())
     return _lib
+
+
+class use_library:
+    """Context manager: route every oracle call through another build of the
+    oracle (a variant with a planted mistake, built by build.build_source),
+    then restore the normal library.  Used only by the tests that check that
+    the pins catch such mistakes."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.saved = lib()
+        _lib = _load(self.path)
+        return _lib
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
 
 
 def _p(a, ctype):

@@ -319,6 +319,124 @@ def test_gate_logits_exact_on_integer_products():
     assert np.array_equal(z, (from_bits(x).astype(np.int64) @ gw.astype(np.int64)).astype(np.float32))
 
 
+def _f32_round(q):
+    """Nearest float32 to the exact rational q, ties to the even significand
+    (IEEE round-to-nearest-even, found by exact comparison -- no double
+    rounding through float64)."""
+    from fractions import Fraction
+    c = np.float32(float(q))
+    best = None
+    for cand in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        dist = abs(Fraction(float(cand)) - q)
+        even = (int(np.asarray(cand, np.float32).view(np.uint32)) & 1) == 0
+        key = (dist, not even)
+        if best is None or key < best[0]:
+            best = (key, cand)
+    return np.float32(best[1])
+
+
+def _fmaf(a, b, c):
+    """fmaf: a*b + c rounded once to float32 (exact rational arithmetic)."""
+    from fractions import Fraction
+    return _f32_round(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
+
+
+def _addf(a, b):
+    from fractions import Fraction
+    return _f32_round(Fraction(float(a)) + Fraction(float(b)))
+
+
+def _logit_in_order(xr, wc, order):
+    """One logit x . w in float32 under a named summation order.
+    "strided32-tree": 32 chains over channels l, l+32, ... (fmaf), then the
+    tree with offsets 16, 8, 4, 2, 1 -- the order the oracle states;
+    the others are plausible misreadings of it."""
+    d = len(xr)
+    zero = np.float32(0.0)
+    if order == "sequential":
+        acc = zero
+        for i in range(d):
+            acc = _fmaf(xr[i], wc[i], acc)
+        return acc
+    if order in ("strided32-tree", "strided32-linear", "strided32-tree-up", "contiguous32-tree", "strided16-tree"):
+        L = 16 if order == "strided16-tree" else 32
+        part = []
+        for l in range(L):
+            acc = zero
+            chans = range(l * (d // L), (l + 1) * (d // L)) if order == "contiguous32-tree" else range(l, d, L)
+            for i in chans:
+                acc = _fmaf(xr[i], wc[i], acc)
+            part.append(acc)
+        if order == "strided32-linear":
+            acc = part[0]
+            for l in range(1, L):
+                acc = _addf(acc, part[l])
+            return acc
+        if order == "strided32-tree-up":                 # adjacent pairs first: (p0+p1), (p2+p3), ...
+            step = 1
+            while step < L:
+                for l in range(0, L, 2 * step):
+                    part[l] = _addf(part[l], part[l + step])
+                step *= 2
+            return part[0]
+        off = L // 2
+        while off >= 1:
+            for l in range(off):
+                part[l] = _addf(part[l], part[l + off])
+            off //= 2
+        return part[0]
+    raise ValueError(order)
+
+
+def test_gate_logits_fixed_order_exactly():
+    """The oracle's logits equal the stated fixed order evaluated with exactly
+    rounded float32 operations (every fused multiply-add and add rounded once,
+    by rational arithmetic), bias added last; and each plausible misreading
+    of the order (one sequential chain, contiguous chunks, 16 chains, a linear
+    or bottom-up sum of the partials) disagrees with the oracle somewhere on
+    the same inputs, so this test tells the orders apart."""
+    rng = np.random.default_rng(61)
+    T, d, E = 3, 256, 4
+    x = bf16_bits_of(rng.normal(0, 1, (T, d)))
+    gw = (rng.normal(0, 1, (d, E)) / math.sqrt(d)).astype(np.float32)
+    bias = rng.normal(0, 1, E).astype(np.float32)
+    xf = from_bits(x)
+    want = np.empty((T, E), np.float32)
+    for t in range(T):
+        for e in range(E):
+            want[t, e] = _addf(_logit_in_order(xf[t], gw[:, e], "strided32-tree"), bias[e])
+    got = oracle.gate_logits(x, gw, bias)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    for order in ("sequential", "contiguous32-tree", "strided16-tree", "strided32-linear", "strided32-tree-up"):
+        alt = np.array([[_addf(_logit_in_order(xf[t], gw[:, e], order), bias[e]) for e in range(E)]
+                        for t in range(T)], np.float32)
+        assert not np.array_equal(alt.view(np.uint32), got.view(np.uint32)), order
+
+
+def test_gate_logits_hand_built_order_case():
+    """A case worked out by hand.  d = 64, one expert, x = 1 on channels 0, 1
+    and 33 (0 elsewhere); gate_w = 1 on channel 0 and b = 2^-24 on channels 1
+    and 33.  In the fixed order, chain 1 holds channels 1 and 33:
+    fmaf(1, b, fmaf(1, b, 0)) = 2b = 2^-23 exactly; chain 0 holds channel 0
+    (= 1); the tree adds chain 1 into chain 0 at the last level (offset 1),
+    after chain 1 has absorbed only zeros (chains 3, 5, 9, 17), giving
+    1 + 2^-23, which is a float32 (one ulp above 1).  A single sequential
+    chain gives 1: 1 + b is a tie between 1 and 1 + 2^-23 and rounds to the
+    even significand, 1, and so does the second b.  Contiguous chunks of
+    two channels put channel 1 beside channel 0 (1 + b -> 1) and channel 33
+    alone in chunk 16, which meets chunk 0 first in the tree (1 + b -> 1):
+    again 1."""
+    d = 64
+    x = np.zeros((1, d), np.float32)
+    x[0, [0, 1, 33]] = 1.0
+    gw = np.zeros((d, 1), np.float32)
+    gw[0, 0] = 1.0
+    gw[[1, 33], 0] = np.float32(2.0 ** -24)
+    z = oracle.gate_logits(bf16_bits_of(x), gw)
+    assert z[0, 0] == np.float32(1.0 + 2.0 ** -23)
+    assert z[0, 0] != np.float32(1.0)
+
+
 def test_topk_bruteforce_and_ties():
     rng = np.random.default_rng(8)
     T, E, k = 200, 32, 6
