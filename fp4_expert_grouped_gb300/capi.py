@@ -27,7 +27,11 @@ STATUS_NAMES = {
 STAGES = ["gate", "topk", "plan", "dispatch", "gemm1", "gemm2", "combine"]
 (MOE_WS_XQ, MOE_WS_XS, MOE_WS_LOGITS, MOE_WS_TOPK_IDX, MOE_WS_TOPK_W, MOE_WS_EXPERT_OFFSETS,
  MOE_WS_SORTED_PAIR, MOE_WS_PAIR_POS, MOE_WS_TILE_PREFIX, MOE_WS_HQ, MOE_WS_HS_TILES, MOE_WS_Y,
- MOE_WS_XQ_SORTED, MOE_WS_XS_TILES, MOE_WS_PLAN_COUNTS, MOE_WS_TILE_DONE, MOE_WS_COUNT) = range(17)
+ MOE_WS_XQ_SORTED, MOE_WS_XS_TILES, MOE_WS_PLAN_COUNTS, MOE_WS_TILE_DONE, MOE_WS_TOPK_Z, MOE_WS_GATE_WT,
+ MOE_WS_GATE_WHI, MOE_WS_GATE_WLO, MOE_WS_GATE_WNORM, MOE_WS_GATE_NCAND, MOE_WS_COUNT) = range(23)
+# from this many tokens (E a multiple of 64) the gate runs on the tensor cores
+# with certified routing (include/fp4moe.h)
+MOE_GATE_TC_MIN_TOKENS = 1024
 
 # every symbol the header declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_fp4_to_fp8t", "moe_quantize_act", "moe_route",

@@ -120,6 +120,13 @@ bool workspace_layout(const Shapes &s, Workspace *ws)
     bytes[MOE_WS_PLAN_COUNTS] = plan_scratch_bytes((long long)P, s.E);
     stride[MOE_WS_PLAN_COUNTS] = (size_t)s.E * 4;
     bytes[MOE_WS_TILE_DONE] = (tiles + 1) * 4; stride[MOE_WS_TILE_DONE] = 4;
+    bytes[MOE_WS_TOPK_Z] = P * 4;            stride[MOE_WS_TOPK_Z] = k * 4;
+    const bool tc = gate_uses_tc(s.T, s.d, s.E);
+    bytes[MOE_WS_GATE_WT] = tc ? E * d * 4 : 0;   stride[MOE_WS_GATE_WT] = d * 4;
+    bytes[MOE_WS_GATE_WHI] = tc ? E * d * 2 : 0;  stride[MOE_WS_GATE_WHI] = d * 2;
+    bytes[MOE_WS_GATE_WLO] = tc ? E * d * 2 : 0;  stride[MOE_WS_GATE_WLO] = d * 2;
+    bytes[MOE_WS_GATE_WNORM] = tc ? E * 4 : 0;    stride[MOE_WS_GATE_WNORM] = 4;
+    bytes[MOE_WS_GATE_NCAND] = tc ? T * 4 : 0;    stride[MOE_WS_GATE_NCAND] = 4;
     size_t off = 0;
     for (int i = 0; i < MOE_WS_COUNT; i++) {
         ws->off[i] = off;
@@ -208,11 +215,34 @@ moe_status moe_route(const uint16_t *x, const float *gate_w, const float *gate_b
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
+    const bool tc = gate_uses_tc(T, d, E);
+    // logits [T][E]; with the tensor-core gate also gate_w transposed (fp32)
+    // and split (two bf16), the weight norms and the candidate counts
+    const size_t zb = round_up((size_t)T * E * 4, 256), wtb = round_up((size_t)E * d * 4, 256),
+                 wpb = round_up((size_t)E * d * 2, 256), wnb = round_up((size_t)E * 4, 256);
+    const size_t bytes = zb + (tc ? wtb + 2 * wpb + wnb + (size_t)T * 4 : 0);
     void *z = nullptr;
-    if (cudaMallocAsync(&z, (size_t)T * E * sizeof(float), s) != cudaSuccess) return MOE_ERR_WORKSPACE;
-    cudaError_t e = launch_gate_logits(x, gate_w, gate_bias, (float *)z, T, d, E, s);
-    if (e == cudaSuccess)
-        e = launch_topk((const float *)z, topk_idx, topk_w, nullptr, nullptr, nullptr, 0, T, d, E, k, di->status, s);
+    if (cudaMallocAsync(&z, bytes, s) != cudaSuccess) return MOE_ERR_WORKSPACE;
+    cudaError_t e;
+    if (tc) {
+        uint8_t *b = static_cast<uint8_t *>(z);
+        GateScratch g;
+        g.approx = reinterpret_cast<float *>(b);
+        g.wt = reinterpret_cast<float *>(b + zb);
+        g.whi = reinterpret_cast<uint16_t *>(b + zb + wtb);
+        g.wlo = reinterpret_cast<uint16_t *>(b + zb + wtb + wpb);
+        g.wn = reinterpret_cast<float *>(b + zb + wtb + 2 * wpb);
+        g.ncand = reinterpret_cast<int32_t *>(b + zb + wtb + 2 * wpb + wnb);
+        e = launch_gate_tc_logits(x, gate_w, gate_bias, g, T, d, E, di->num_sms, di->status, timeout_ns(), s);
+        if (e == cudaSuccess)
+            e = launch_gate_certify(x, gate_bias, g, topk_idx, topk_w, nullptr, nullptr, nullptr, 0, T, d, E, k,
+                                    di->status, s);
+    } else {
+        e = launch_gate_logits(x, gate_w, gate_bias, (float *)z, T, d, E, s);
+        if (e == cudaSuccess)
+            e = launch_topk((const float *)z, topk_idx, topk_w, nullptr, nullptr, nullptr, 0, T, d, E, k, di->status,
+                            s);
+    }
     cudaError_t f = cudaFreeAsync(z, s);
     return cuda_status(e != cudaSuccess ? e : f);
 }
@@ -308,11 +338,30 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     auto mark = [&](int stage) {
         if (o.stage_events && e == cudaSuccess) e = cudaEventRecord((cudaEvent_t)o.stage_events[stage], s);
     };
+    float *topk_z = reinterpret_cast<float *>(at(MOE_WS_TOPK_Z));
     mark(MOE_STAGE_GATE);
-    if (e == cudaSuccess) e = launch_gate_logits(x, gate_w, o.gate_bias, logits, T, d, E, s);
-    mark(MOE_STAGE_TOPK);
-    if (e == cudaSuccess)
-        e = launch_topk(logits, topk_idx, topk_w, x, xq, xs, xs_stride, T, d, E, k, di->status, s);
+    if (gate_uses_tc(T, d, E)) {
+        // tensor-core logits, then (the top-k stage) the certified top-k with
+        // the candidates' fixed-order logits and the FP8 quantisation of x
+        GateScratch gs;
+        gs.wt = reinterpret_cast<float *>(at(MOE_WS_GATE_WT));
+        gs.whi = reinterpret_cast<uint16_t *>(at(MOE_WS_GATE_WHI));
+        gs.wlo = reinterpret_cast<uint16_t *>(at(MOE_WS_GATE_WLO));
+        gs.wn = reinterpret_cast<float *>(at(MOE_WS_GATE_WNORM));
+        gs.approx = logits;
+        gs.ncand = reinterpret_cast<int32_t *>(at(MOE_WS_GATE_NCAND));
+        if (e == cudaSuccess)
+            e = launch_gate_tc_logits(x, gate_w, o.gate_bias, gs, T, d, E, di->num_sms, di->status, timeout_ns(), s);
+        mark(MOE_STAGE_TOPK);
+        if (e == cudaSuccess)
+            e = launch_gate_certify(x, o.gate_bias, gs, topk_idx, topk_w, topk_z, xq, xs, xs_stride, T, d, E, k,
+                                    di->status, s);
+    } else {
+        if (e == cudaSuccess) e = launch_gate_logits(x, gate_w, o.gate_bias, logits, T, d, E, s);
+        mark(MOE_STAGE_TOPK);
+        if (e == cudaSuccess)
+            e = launch_topk(logits, topk_idx, topk_w, x, xq, xs, xs_stride, T, d, E, k, di->status, s, topk_z);
+    }
     mark(MOE_STAGE_PLAN);
     if (e == cudaSuccess)
         e = launch_plan(topk_idx, offs, sorted_pair, pair_pos, tile_prefix,

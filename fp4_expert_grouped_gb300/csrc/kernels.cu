@@ -649,7 +649,8 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
 // groups' loads are in flight together rather than one after another.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void topk_warp(const float *__restrict__ zt, int32_t *__restrict__ idx_out,
-                                          float *__restrict__ w_out, int E, int k, unsigned *status)
+                                          float *__restrict__ w_out, float *__restrict__ z_out, int E, int k,
+                                          unsigned *status)
 {
     const int lane = threadIdx.x & 31;
     float v[8];
@@ -717,6 +718,7 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ zt, int32_t 
     if (lane < k) {
         idx_out[lane] = my_e;
         w_out[lane] = (S == 0.f) ? 1.0f / (float)k : s / S;
+        if (z_out) z_out[lane] = my_z;
     }
 }
 
@@ -726,12 +728,14 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float *__re
                                                                float *__restrict__ topk_w, const uint16_t *__restrict__ x,
                                                                uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
                                                                int xs_stride, int T, int d, int E, int k,
-                                                               unsigned *status)
+                                                               unsigned *status, float *__restrict__ topk_z)
 {
     pdl_wait();
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == 0) topk_warp(z + (size_t)t * E, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, E, k, status);
+    if (warp == 0)
+        topk_warp(z + (size_t)t * E, topk_idx + (size_t)t * k, topk_w + (size_t)t * k,
+                  topk_z ? topk_z + (size_t)t * k : nullptr, E, k, status);
     if (!xq) return;
     const uint16_t *xrow = x + (size_t)t * d;
     uint8_t *qrow = xq + (size_t)t * d;
@@ -754,25 +758,27 @@ __global__ void __launch_bounds__(256) topk_warp_per_token_kernel(const float *_
                                                                   const uint16_t *__restrict__ x,
                                                                   uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
                                                                   int xs_stride, int T, int d, int E, int k,
-                                                                  unsigned *status)
+                                                                  unsigned *status, float *__restrict__ topk_z)
 {
     pdl_wait();
     const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (t >= T) return;
-    topk_warp(z + (size_t)t * E, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, E, k, status);
+    topk_warp(z + (size_t)t * E, topk_idx + (size_t)t * k, topk_w + (size_t)t * k,
+              topk_z ? topk_z + (size_t)t * k : nullptr, E, k, status);
     if (xq) quant_row_warp(x + (size_t)t * d, xq + (size_t)t * d, xs + (size_t)t * xs_stride, d, xs_stride);
     pdl_trigger();
 }
 
 cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const uint16_t *x, uint8_t *xq,
-                        uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st)
+                        uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st,
+                        float *topk_z)
 {
     if (T == 0) return cudaSuccess;
     if (T >= 2048)
         return launch_pdl(topk_warp_per_token_kernel, dim3((T + 7) / 8), dim3(256), 0, st, z, topk_idx, topk_w, x, xq,
-                          xs, xs_stride, T, d, E, k, status);
+                          xs, xs_stride, T, d, E, k, status, topk_z);
     return launch_pdl(topk_kernel, dim3(T), dim3(kTopkWarps * 32), 0, st, z, topk_idx, topk_w, x, xq, xs, xs_stride, T,
-                      d, E, k, status);
+                      d, E, k, status, topk_z);
 }
 
 // ---------------------------------------------------------------------------

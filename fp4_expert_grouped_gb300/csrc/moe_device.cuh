@@ -293,6 +293,19 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A x B^T with bf16 A and B from shared-memory descriptors and an
+// fp32 accumulator (kind::f16: both operands of the same 16-bit type).
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 {
@@ -323,6 +336,20 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset: 8 rows x 128 B
     d |= (uint64_t)1 << 46;                             // descriptor version
     d |= (uint64_t)2 << 61;                             // layout: 128-byte swizzle
+    return d;
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored with the
+// 64-byte swizzle: rows of 64 bytes, 8-row atoms 512 bytes apart (the tile
+// 512-byte aligned).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                             // leading byte offset (unused here)
+    d |= (uint64_t)(512u >> 4) << 32;                   // stride byte offset: 8 rows x 64 B
+    d |= (uint64_t)1 << 46;                             // descriptor version
+    d |= (uint64_t)4 << 61;                             // layout: 64-byte swizzle
     return d;
 }
 

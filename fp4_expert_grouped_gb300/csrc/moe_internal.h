@@ -54,8 +54,8 @@ struct Shapes {
 
 // Workspace layout (byte offsets, row strides).
 struct Workspace {
-    size_t off[16];
-    size_t stride[16];
+    size_t off[32];
+    size_t stride[32];
     size_t total;
 };
 bool workspace_layout(const Shapes &s, Workspace *ws);
@@ -120,7 +120,8 @@ cudaError_t launch_gate_logits(const uint16_t *x, const float *gate_w, const flo
 // top-k + weights for every token; optionally quantises x in the same pass
 // (xq/xs may be NULL).
 cudaError_t launch_topk(const float *z, int32_t *topk_idx, float *topk_w, const uint16_t *x, uint8_t *xq,
-                        uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st);
+                        uint8_t *xs, int xs_stride, int T, int d, int E, int k, unsigned *status, cudaStream_t st,
+                        float *topk_z = nullptr);
 // dispatch plan; tile_prefix may be NULL.  cta_counts: plan_scratch_bytes()
 // of scratch for large P (NULL runs the plan as one CTA whatever P).
 // With xs_tiles, also writes every pair's token scales (xs [T][xs_stride],
@@ -145,6 +146,34 @@ cudaError_t launch_dispatch_dense(const uint8_t *xq, const int32_t *pair_pos, co
                                   cudaStream_t st);
 cudaError_t launch_combine(const uint16_t *y, const int32_t *pair_pos, const float *topk_w, uint16_t *out, int T,
                            int d, int k, cudaStream_t st);
+
+// ---- tensor-core gate with certified routing (gate_tc.cu) -----------------
+// Batches of at least kGateTcMinTokens tokens (E a multiple of 64, at most
+// 256) compute approximate logits on the tensor cores and then the exact
+// fixed-order logits of the candidate experts only; the routing is the same
+// bits either way.
+constexpr long long kGateTcMinTokens = 1024;
+bool gate_uses_tc(long long T, int d, int E);
+// c(d) of the bound |approx - fixed-order logit| <= c(d) ||x|| ||w_e|| + 2^-22 |approx|
+float gate_bound_coefficient(int d);
+struct GateScratch {
+    float *wt;          // fp32 [E][d]: gate_w transposed
+    uint16_t *whi;      // bf16 [E][d]: its high parts
+    uint16_t *wlo;      // bf16 [E][d]: w - hi rounded to bf16
+    float *wn;          // fp32 [E]: upper bounds of the experts' weight norms
+    float *approx;      // fp32 [T][E]: tensor-core logits (+ bias)
+    int32_t *ncand;     // int32 [T]: candidate experts per token (or NULL)
+};
+// the tensor-core logits: gate_w split and transposed, the weight norms, then
+// g.approx = x . (hi + lo) + bias
+cudaError_t launch_gate_tc_logits(const uint16_t *x, const float *gate_w, const float *bias, const GateScratch &g,
+                                  int T, int d, int E, int num_sms, unsigned *status, unsigned long long timeout_ns,
+                                  cudaStream_t st);
+// then the certified top-k (+ FP8 quantisation of x when xq is given);
+// topk_z (or NULL): the selected experts' fixed-order logits
+cudaError_t launch_gate_certify(const uint16_t *x, const float *bias, const GateScratch &g, int32_t *topk_idx,
+                                float *topk_w, float *topk_z, uint8_t *xq, uint8_t *xs, int xs_stride, int T, int d,
+                                int E, int k, unsigned *status, cudaStream_t st);
 
 // ---- grouped GEMMs (gemm.cu) ---------------------------------------------
 struct GemmArgs {

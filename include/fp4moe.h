@@ -142,7 +142,9 @@ moe_status moe_quantize_act(const uint16_t *x, uint8_t *xq, uint8_t *xs,
  * (t, e), 32 partial sums over channels i = l, l+32, ... accumulated with fused
  * multiply-adds in increasing i, then added as a binary tree with offsets
  * 16, 8, 4, 2, 1 (partial[l] += partial[l + off]); the bias is added last.
- * Inputs must be finite.  Allocates T*E*4 bytes of stream-ordered scratch.
+ * Inputs must be finite.  Allocates stream-ordered scratch: T*E*4 bytes, plus
+ * E*d*8 + E*4 + T*4 bytes from MOE_GATE_TC_MIN_TOKENS tokens on (the
+ * tensor-core gate below, which gives the same routing bits).
  */
 moe_status moe_route(const uint16_t *x, const float *gate_w, const float *gate_bias,
                      int32_t *topk_idx, float *topk_w, int T, int d, int E, int k, void *stream);
@@ -261,7 +263,11 @@ size_t moe_workspace_size(int T, int d, int inter, int E, int k);
 enum {
     MOE_WS_XQ = 0,        /* uint8 E4M3 [T][d] */
     MOE_WS_XS,            /* uint8 [T][stride], first d/128 bytes of a row used */
-    MOE_WS_LOGITS,        /* fp32 [T][E] */
+    MOE_WS_LOGITS,        /* fp32 [T][E]: below MOE_GATE_TC_MIN_TOKENS tokens (or E not a
+                             multiple of 64) the fixed-order logits; from there on the
+                             tensor-core approximations a, each within
+                             c(d) ||x_t|| ||w_e|| + 2^-22 |a| + d 2^-125 of the
+                             fixed-order logit (the gate path below) */
     MOE_WS_TOPK_IDX,      /* int32 [T][k] */
     MOE_WS_TOPK_W,        /* fp32 [T][k] */
     MOE_WS_EXPERT_OFFSETS,/* int32 [E+1] */
@@ -285,8 +291,31 @@ enum {
     MOE_WS_TILE_DONE,     /* int32 per GEMM row tile: GEMM1 epilogue warps that have stored
                              the tile's hq rows and scales (GEMM2 starts a row tile once all
                              of them have), then one int32 total over all tiles */
+    MOE_WS_TOPK_Z,        /* fp32 [T][k]: the fixed-order logits of the selected experts */
+    /* the tensor-core gate's scratch (empty below MOE_GATE_TC_MIN_TOKENS tokens): */
+    MOE_WS_GATE_WT,       /* fp32 [E][d]: gate_w transposed */
+    MOE_WS_GATE_WHI,      /* bf16 [E][d]: its high parts (round to nearest even) */
+    MOE_WS_GATE_WLO,      /* bf16 [E][d]: w - hi, rounded to bf16 */
+    MOE_WS_GATE_WNORM,    /* fp32 [E]: upper bounds of ||w_e||_2 */
+    MOE_WS_GATE_NCAND,    /* int32 [T]: experts whose logit was computed in the fixed
+                             order (the candidates of the certified top-k) */
     MOE_WS_COUNT
 };
+
+/* Gate path.  From this many tokens on (with E a multiple of 64, at most
+ * 256), the logits are first approximated on the tensor cores: gate_w is
+ * split into bf16 parts hi + lo (|w - hi - lo| <= 2^-16 |w|) and
+ * a = x . (hi + lo) + bias is accumulated in fp32, restarting every 128
+ * channels.  Each a_e lies within D_e = c(d) ||x_t|| ||w_e|| + 2^-22 |a_e| +
+ * d 2^-125 of the fixed-order logit z_e (c(d) = 1.026 (2^-16 + 17 * 2^-17 +
+ * (5 d/128 + 5) 2^-24): the split, 16 MMAs per chunk at 2^-17 each, the chunk
+ * sums, the fixed order's own rounding; the last term, products flushed below
+ * the normal range).  Every expert of the exact top-k has
+ * a_e + D_e >= L, the k-th largest a_e - D_e; for those candidates alone the
+ * fixed-order logit is computed, and the top-k, its slot order and the
+ * weights come from those.  The routing is therefore bit-identical to the
+ * CUDA-core path's for every token, whatever the batch. */
+#define MOE_GATE_TC_MIN_TOKENS 1024
 size_t moe_workspace_layout(int T, int d, int inter, int E, int k,
                             size_t *offsets, size_t *strides);
 

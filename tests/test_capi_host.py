@@ -120,9 +120,11 @@ def test_workspace_layout(capi):
         tiles = (P + R - 1) // R + min(P, E)
         gx, gh = (d // 128 + 3) // 4, (inter // 128 + 3) // 4
         chunks = (P + 2047) // 2048
+        tc = T >= capi.MOE_GATE_TC_MIN_TOKENS and E % 64 == 0         # the tensor-core gate's scratch
         sizes = [T * d, T * xs, T * E * 4, P * 4, P * 4, (E + 1) * 4, P * 4, P * 4, (E + 1) * 4,
                  P * inter, tiles * gh * 512, P * d * 2, P * d, tiles * gx * 512,
-                 chunks * E * 4 if chunks > 1 else 0, (tiles + 1) * 4]
+                 chunks * E * 4 if chunks > 1 else 0, (tiles + 1) * 4, P * 4,
+                 E * d * 4 * tc, E * d * 2 * tc, E * d * 2 * tc, E * 4 * tc, T * 4 * tc]
         assert len(sizes) == capi.MOE_WS_COUNT
         for i in range(capi.MOE_WS_COUNT):
             assert off[i] % 256 == 0

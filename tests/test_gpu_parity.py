@@ -344,9 +344,40 @@ def test_forward_full_size_sampled_tokens(name, workload_cache):
     oi, ow = oracle.topk(z, w.k)
     assert np.array_equal(ti.cpu().numpy(), oi)
     assert np.allclose(tw.cpu().numpy(), ow, rtol=2e-7, atol=0)
-    _, off, _ = capi().moe_workspace_layout(w.T, w.d, w.inter, w.E, w.k)
-    zl = ws[off[capi().MOE_WS_LOGITS]:][:4 * w.T * w.E].view(torch.int32).cpu().numpy().reshape(w.T, w.E)
-    assert np.array_equal(zl, z.view(np.int32))
+    check_gate_workspace(ws, w, x, gw, z, oi)
+
+
+def gate_bound_coefficient(d):
+    """c(d) of the bound |a - z| <= c(d) ||x|| ||w_e|| + 2^-22 |a| + d 2^-125
+    the library states for its tensor-core logits a (include/fp4moe.h, gate path)."""
+    u = 2.0 ** -24
+    return (2.0 ** -16 + 17 * 2.0 ** -17 + (5 * d / 128 + 5) * u) * (1 + 2.0 ** -6) * 1.01
+
+
+def check_gate_workspace(ws, w, x, gw, z, oi, what=""):
+    """The gate's workspace against the oracle's fixed-order logits z: the
+    selected experts' logits bit for bit; the logits region bit for bit on the
+    CUDA-core path, within the stated bound on the tensor-core path (where
+    the bound must hold for every token and expert, since the routing is
+    certified by it).  Returns the largest |a - z| / (c(d) ||x|| ||w_e||)."""
+    c = capi()
+    _, off, _ = c.moe_workspace_layout(w.T, w.d, w.inter, w.E, w.k)
+    tz = ws[off[c.MOE_WS_TOPK_Z]:][:4 * w.T * w.k].view(torch.float32).cpu().numpy().reshape(w.T, w.k)
+    assert np.array_equal(tz.view(np.int32), np.take_along_axis(z, oi, 1).view(np.int32)), what
+    a = ws[off[c.MOE_WS_LOGITS]:][:4 * w.T * w.E].view(torch.float32).cpu().numpy().reshape(w.T, w.E)
+    if w.T < c.MOE_GATE_TC_MIN_TOKENS or w.E % 64:
+        assert np.array_equal(a.view(np.int32), z.view(np.int32)), what
+        return 0.0
+    xf = f32(inputs.bf16_bits(x)).reshape(w.T, w.d)
+    xn = np.linalg.norm(xf, axis=1)
+    wn = np.linalg.norm(gw.cpu().numpy().astype(np.float64), axis=0)
+    cs = gate_bound_coefficient(w.d) * xn[:, None] * wn[None, :]
+    err = np.abs(a.astype(np.float64) - z.astype(np.float64))
+    assert np.all(err <= cs + 2.0 ** -22 * np.abs(a) + w.d * 2.0 ** -125), (what, float((err / cs).max()))
+    nc = ws[off[c.MOE_WS_GATE_NCAND]:][:4 * w.T].view(torch.int32).cpu().numpy()
+    assert np.all(nc >= w.k) and np.all(nc <= w.E), what
+    live = cs > 0                                   # rows of zeros have no main term
+    return float((err[live] / cs[live]).max()) if live.any() else 0.0
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "mid", "skew", "prefill"])
