@@ -337,41 +337,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // The token's bf16 row, 8 channels per lane and step, quantised to E4M3 with
 // one power-of-two scale per 128 channels when qrow is given (two groups per
 // step, one per half-warp: the rule of moe_quantize_act); returns this lane's
-// part of the row's sum of squares.
+// part of the row's sum of squares.  The row is read eight steps (8 KB) at a
+// time, all loads in flight together: the row comes from DRAM, and one
+// dependent load per step made this the longest part of a token's work.
 __device__ __forceinline__ float quant_row_ssq(const uint16_t *__restrict__ xrow, uint8_t *__restrict__ qrow,
                                                uint8_t *__restrict__ srow, int d, int s_stride)
 {
+    constexpr int B = 8;
     const int lane = threadIdx.x & 31;
     const int n8 = d / 8;
     const uint4 *src = reinterpret_cast<const uint4 *>(xrow);
     float ssq = 0.f;
-    for (int c = lane; c - lane < n8; c += 32) {
-        uint4 cur = make_uint4(0, 0, 0, 0);
-        if (c < n8) cur = __ldg(src + c);
-        const uint32_t u[4] = {cur.x, cur.y, cur.z, cur.w};
-        float v[8];
+    for (int c0 = 0; c0 < n8; c0 += 32 * B) {
+        uint4 cur[B];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            v[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
-            v[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
+        for (int b = 0; b < B; b++) {
+            const int c = c0 + 32 * b + lane;
+            cur[b] = c < n8 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
         }
-        float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            amax = fmaxf(amax, fabsf(v[i]));
-            ssq = fmaf(v[i], v[i], ssq);
-        }
-        if (qrow) {
+        for (int b = 0; b < B; b++) {
+            const int c = c0 + 32 * b + lane;
+            if (c0 + 32 * b >= n8) break;                  // warp-uniform
+            const uint32_t u[4] = {cur[b].x, cur[b].y, cur[b].z, cur[b].w};
+            float v[8];
 #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-            if (c < n8) {
-                const int e = e4m3_scale_exp(amax);
-                const float sc = exp2i(-e);
-                uint2 q;
-                q.x = cvt_e4m3x2(v[0] * sc, v[1] * sc) | (cvt_e4m3x2(v[2] * sc, v[3] * sc) << 16);
-                q.y = cvt_e4m3x2(v[4] * sc, v[5] * sc) | (cvt_e4m3x2(v[6] * sc, v[7] * sc) << 16);
-                reinterpret_cast<uint2 *>(qrow)[c] = q;
-                if ((lane & 15) == 0) srow[c / 16] = (uint8_t)(e + 127);
+            for (int i = 0; i < 4; i++) {
+                v[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
+                v[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                amax = fmaxf(amax, fabsf(v[i]));
+                ssq = fmaf(v[i], v[i], ssq);
+            }
+            if (qrow) {
+#pragma unroll
+                for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                if (c < n8) {
+                    const int e = e4m3_scale_exp(amax);
+                    const float sc = exp2i(-e);
+                    uint2 q;
+                    q.x = cvt_e4m3x2(v[0] * sc, v[1] * sc) | (cvt_e4m3x2(v[2] * sc, v[3] * sc) << 16);
+                    q.y = cvt_e4m3x2(v[4] * sc, v[5] * sc) | (cvt_e4m3x2(v[6] * sc, v[7] * sc) << 16);
+                    reinterpret_cast<uint2 *>(qrow)[c] = q;
+                    if ((lane & 15) == 0) srow[c / 16] = (uint8_t)(e + 127);
+                }
             }
         }
     }
