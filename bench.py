@@ -216,14 +216,20 @@ def gemm_flops(w, which):
     return 2 * w.P * w.d * (2 * w.inter if which == "gemm1" else w.inter)
 
 
+GATE_TC_MIN_TOKENS = 1024      # the library's tensor-core gate threshold (include/fp4moe.h)
+
+
 def kernels_per_step(w):
-    """Kernels the library launches for one forward of workload w: gate,
-    top-k, the dispatch plan (a count and a scatter kernel beyond 32768 pairs,
-    one kernel up to that), the expert-ordered copy (from 16 pairs per expert
-    on average), GEMM1, GEMM2, combine."""
+    """Kernels the library launches for one forward of workload w: the gate
+    and top-k (two kernels below 1024 tokens; from there, with E a multiple of
+    64, four: gate_w split, weight norms, tensor-core logits, certified
+    top-k), the dispatch plan (a count and a scatter kernel beyond 32768
+    pairs, one kernel up to that), the expert-ordered copy (from 16 pairs per
+    expert on average), GEMM1, GEMM2, combine."""
+    gate = 4 if w.T >= GATE_TC_MIN_TOKENS and w.E % 64 == 0 else 2
     plan = 2 if w.P > 32768 else 1
     dispatch = 1 if w.P >= 16 * w.E else 0
-    return 2 + plan + dispatch + 3
+    return gate + plan + dispatch + 3
 
 
 def layer_roofline(w, touched, hbm_gbs, fp8_tflops):

@@ -30,18 +30,24 @@ def test_flop_identity_matches_cited_ratio():
 
 
 def test_kernels_per_step_follow_the_library_thresholds():
-    """gpu_launches claim: gate, top-k, plan (one kernel up to 32768 pairs, a
-    count and a scatter kernel above), the expert-ordered copy (from 16 pairs
-    per expert on average), GEMM1, GEMM2, combine."""
-    want = {"tiny": 6, "decode": 6, "mid": 7, "skew": 8, "prefill": 8}
+    """gpu_launches claim: the gate and top-k (two kernels, or four on the
+    tensor-core path from 1024 tokens with E a multiple of 64), plan (one
+    kernel up to 32768 pairs, a count and a scatter kernel above), the
+    expert-ordered copy (from 16 pairs per expert on average), GEMM1, GEMM2,
+    combine."""
+    want = {"tiny": 6, "decode": 6, "mid": 9, "skew": 10, "prefill": 10}
     for name, n in want.items():
         assert bench.kernels_per_step(inputs.WORKLOADS[name]) == n, name
     edge = inputs.Workload("edge", T=4096, d=256, inter=128, E=256, k=8, seed=0)    # 32768 pairs: one plan kernel
-    assert bench.kernels_per_step(edge) == 7
+    assert bench.kernels_per_step(edge) == 9
     edge = inputs.Workload("edge", T=4097, d=256, inter=128, E=256, k=8, seed=0)    # 32776 pairs: two
-    assert bench.kernels_per_step(edge) == 8
+    assert bench.kernels_per_step(edge) == 10
     edge = inputs.Workload("edge", T=511, d=256, inter=128, E=256, k=8, seed=0)     # 4088 < 16 E: no copy
     assert bench.kernels_per_step(edge) == 6
+    edge = inputs.Workload("edge", T=1023, d=256, inter=128, E=256, k=8, seed=0)    # below the tensor-core gate
+    assert bench.kernels_per_step(edge) == 7
+    edge = inputs.Workload("edge", T=2048, d=256, inter=128, E=40, k=8, seed=0)     # E not a multiple of 64
+    assert bench.kernels_per_step(edge) == 7
 
 
 def test_clock_window_keeps_the_gpu_busy_for_the_sampler():
