@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--fp8t", action="store_true",
                     help="instead of the layer: time moe_fp4_to_fp8t (FP8 weights for the backward pass) on "
                          "the workload's W13 and W2 shapes and print one JSON line per matrix")
+    ap.add_argument("--dgrad", action="store_true",
+                    help="instead of the layer: time moe_backward_h (the backward's dh = W2^T dy GEMM with the "
+                         "SwiGLU backward, QAT) on the workload, against its FP8 tensor-core roofline")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (a smaller case of the workload, e.g. for an ncu capture)")
     ap.add_argument("--experts", type=int, default=None,
@@ -551,6 +554,57 @@ def run_fp8t(args, w):
         torch.cuda.empty_cache()
 
 
+def run_dgrad(args, w):
+    """Device time of moe_backward_h on workload w: the forward runs once (keeping
+    g and u), W2 is converted to its FP8 backward weights, then K timed calls
+    (CUDA events, L2 flushed before each) of the three kernels: block-exponent
+    scale image, dy dispatch + E4M3, and the grouped FP8 GEMM with the SwiGLU
+    backward.  Roofline: 2 P d I FLOPs per call at the FP8 peak."""
+    from fp4_expert_grouped_gb300 import capi, inputs, layer
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_gbs, bf16_tflops, _, peak_src = measured_peaks()
+    fp8_tflops = bf16_tflops * FP8_OVER_BF16
+    x, gw, bias = inputs.make_x_gate(w, dev)
+    pk = layer.pack_workload(w, dev)
+    ws = layer.workspace(w.T, w.d, w.inter, w.E, w.k, dev)
+    gu = torch.empty((w.P, 2 * w.inter), dtype=torch.float32, device=dev)
+    layer.forward(x, gw, pk, w.k, gate_bias=bias, ws=ws, gu_out=gu)
+    w8 = torch.empty((w.E, w.inter, w.d), dtype=torch.uint8, device=dev)
+    s8 = torch.empty((w.E, w.inter // 128, w.d // 128), dtype=torch.uint8, device=dev)
+    capi.moe_fp4_to_fp8t(pk.w2_fp4, pk.w2_scale, w8, s8)
+    g = torch.Generator(device=dev).manual_seed(w.seed + 7)
+    dout = torch.randn((w.T, w.d), device=dev, generator=g).to(torch.bfloat16)
+    dgu = torch.empty((w.P, 2 * w.inter), dtype=torch.uint8, device=dev)
+    dgs = torch.empty((w.P, 2 * w.inter // 128), dtype=torch.uint8, device=dev)
+    bws = torch.empty(capi.moe_backward_h_workspace_size(w.T, w.d, w.inter, w.E, w.k), dtype=torch.uint8,
+                      device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        capi.moe_backward_h(dout, w8, s8, gu, ws, dgu, dgs, w.k, workspace=bws)
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        capi.moe_backward_h(dout, w8, s8, gu, ws, dgu, dgs, w.k, workspace=bws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    st = capi.moe_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status: " + capi.moe_status_string(st))
+    t = statistics.median(ms)
+    flops = 2.0 * w.P * w.d * w.inter
+    tf = flops / (t / 1e3) / 1e12
+    print(json.dumps({"metric": "moe_backward_h throughput (dh = W2^T dy + SwiGLU backward, FP8)",
+                      "config": config_of(w), "ms": t, "flops": flops, "value": tf, "unit": "TFLOP/s",
+                      "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_tflops, "unit": "TFLOP/s",
+                                   "peak_note": "FP8 = %.1f x %s bf16 burst" % (FP8_OVER_BF16, peak_src),
+                                   "frac": tf / fp8_tflops}}), flush=True)
+
+
 def main():
     args = parse()
     from fp4_expert_grouped_gb300 import inputs
@@ -562,6 +616,9 @@ def main():
         w = dataclasses.replace(w, name="%s[T=%d,E=%d]" % (w.name, T, E), T=T, E=E)
     if args.fp8t:
         run_fp8t(args, w)
+        return
+    if args.dgrad:
+        run_dgrad(args, w)
         return
     world, rank, local = dist_setup(want_nccl=(args.impl == "ours"))
     if args.impl == "reference":

@@ -36,14 +36,15 @@ MOE_GATE_TC_MIN_TOKENS = 1024
 # every symbol the header declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_fp4_to_fp8t", "moe_quantize_act", "moe_route",
            "moe_route_noalloc", "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
-           "moe_workspace_layout", "moe_get_device_status"]
+           "moe_workspace_layout", "moe_get_device_status", "moe_backward_h", "moe_backward_h_workspace_size"]
 
 
 class MoeForwardOpts(ctypes.Structure):
     _fields_ = [("gate_bias", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("topk_idx_out", ctypes.c_void_p),
                 ("topk_w_out", ctypes.c_void_p), ("pair_pos_out", ctypes.c_void_p),
-                ("flags", ctypes.c_uint32), ("stage_events", ctypes.POINTER(ctypes.c_void_p))]
+                ("flags", ctypes.c_uint32), ("stage_events", ctypes.POINTER(ctypes.c_void_p)),
+                ("gu_out", ctypes.c_void_p)]
 
 
 _vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -74,6 +75,10 @@ _lib.moe_workspace_layout.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(_sz), c
 _lib.moe_workspace_layout.restype = _sz
 _lib.moe_get_device_status.argtypes = [_vp]
 _lib.moe_get_device_status.restype = _i
+_lib.moe_backward_h_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+_lib.moe_backward_h_workspace_size.restype = _sz
+_lib.moe_backward_h.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+_lib.moe_backward_h.restype = _i
 
 
 class MoeError(RuntimeError):
@@ -181,7 +186,7 @@ def moe_forward(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stream=
 
 def moe_forward_ex(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stream=None, gate_bias=None,
                    workspace=None, topk_idx_out=None, topk_w_out=None, pair_pos_out=None, flags=0,
-                   stage_events=None):
+                   stage_events=None, gu_out=None):
     """stage_events: optional list of len(STAGES) + 1 recorded torch.cuda.Event objects."""
     T, d = x.shape
     E = gate_w.shape[1]
@@ -193,10 +198,28 @@ def moe_forward_ex(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stre
     o = MoeForwardOpts(_ptr(gate_bias), _ptr(workspace),
                        0 if workspace is None else workspace.numel() * workspace.element_size(),
                        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(pair_pos_out), flags,
-                       ctypes.cast(evs, ctypes.POINTER(ctypes.c_void_p)) if evs is not None else None)
+                       ctypes.cast(evs, ctypes.POINTER(ctypes.c_void_p)) if evs is not None else None,
+                       _ptr(gu_out))
     _check(_lib.moe_forward_ex(_ptr(x), _ptr(gate_w), _ptr(w13_fp4), _ptr(w13_scale), _ptr(w2_fp4),
                                _ptr(w2_scale), _ptr(out), T, d, inter, E, k, _stream(stream),
                                ctypes.byref(o)), "moe_forward_ex")
+
+
+def moe_backward_h_workspace_size(T, d, inter, E, k):
+    return _lib.moe_backward_h_workspace_size(T, d, inter, E, k)
+
+
+def moe_backward_h(dout, w2_fp8t, w2_s8t, gu, fwd_workspace, dgu, dgu_scale, k, dgu_f32=None, workspace=None,
+                   stream=None):
+    """dout bf16 [T, d], w2_fp8t uint8 [E, inter, d] + w2_s8t [E, inter/128, d/128] (moe_fp4_to_fp8t
+    of W2), gu fp32 [T*k, 2*inter] (moe_forward_ex gu_out), fwd_workspace: that forward's workspace;
+    outputs dgu uint8 [T*k, 2*inter] (E4M3), dgu_scale uint8 [T*k, 2*inter/128], optionally dgu_f32."""
+    T, d = dout.shape
+    E, inter, _ = w2_fp8t.shape
+    _check(_lib.moe_backward_h(_ptr(dout), _ptr(w2_fp8t), _ptr(w2_s8t), _ptr(gu), _ptr(fwd_workspace),
+                               _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+                               _ptr(dgu), _ptr(dgu_scale), _ptr(dgu_f32), T, d, inter, E, k, _stream(stream)),
+           "moe_backward_h")
 
 
 def moe_get_device_status(stream=None):

@@ -299,7 +299,7 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     if (o.flags & ~MOE_FLAG_TEST_STALL_GEMM2) return MOE_ERR_INVALID_ARG;
     if (o.gate_bias && !aligned(o.gate_bias, 4)) return MOE_ERR_INVALID_ARG;
     if ((o.topk_idx_out && !aligned(o.topk_idx_out, 4)) || (o.topk_w_out && !aligned(o.topk_w_out, 4)) ||
-        (o.pair_pos_out && !aligned(o.pair_pos_out, 4)))
+        (o.pair_pos_out && !aligned(o.pair_pos_out, 4)) || (o.gu_out && !aligned(o.gu_out, 32)))
         return MOE_ERR_INVALID_ARG;
     if (!layer_shape_ok(T, d, inter, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
     Workspace ws;
@@ -404,7 +404,9 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
         g.K = d;
         g.hq = hq;
         g.hs_tiles = hs_tiles;
+        g.gu_out = o.gu_out;
         e = launch_gemm1(g, inter, s);
+        g.gu_out = nullptr;
     }
     mark(MOE_STAGE_GEMM2);
     if (e == cudaSuccess) {

@@ -1,0 +1,229 @@
+// backward.cu -- the first GEMM of the MoE layer's backward pass in FP4
+// quantisation-aware training, and its C ABI entry (moe_backward_h).
+//
+// "DeepSeek-V4揭秘：细粒度专家并行隐藏通信时延，FP4量化与TileLang协同优化百万Token上下文"
+// (itsolotime.com/archives/32374), section 4: the backward computes with the
+// FP8 weights the FP4 weights dequantise to (moe_fp4_to_fp8t), transposed
+// 128 x 128 blocks without re-quantisation.  Per token-expert pair p (token t,
+// slot j, expert e), in the forward's expert order:
+//   dy_p       = w_tj dout_t                      (the gradient at y_p)
+//   dyq_p      = E4M3 of dy_p, one power-of-two scale per 128 channels
+//   dh_p       = W2[e]^T dyq_p                    (FP8 x FP8 block-scaled MMA)
+//   dg, du     = the SwiGLU backward with the forward's g, u
+//   [dg; du]   = E4M3, one power-of-two scale per 128 channels
+// Section 3.2 (determinism): no atomics, every sum in a fixed order.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+#include <cstring>
+
+namespace fp4moe {
+
+// The weights' block exponents as the tensor cores' scale-factor image: for
+// expert e, 256-row block nb of W2^T ([inter][d]) and K block ks, two 512-byte
+// blocks (rows 0-127 and 128-255) at ((e * inter/256 + nb) * d/128 + ks) * 2 + h,
+// every byte of block h the exponent of 128 x 128 block (2 nb + h, ks) -- the
+// tiled scale layout of moe_pack_fp4 with N = inter, K = d, all four 1 x 32
+// scales of a row equal.  One thread per 16 bytes.
+__global__ void __launch_bounds__(256) bwd_scale_image_kernel(const uint8_t *__restrict__ s8t, uint8_t *__restrict__ img,
+                                                              long long n16, int inter, int d)
+{
+    pdl_wait();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n16) {
+        const long long b = i / 32;                       // 512-byte block
+        const int h = (int)(b & 1);
+        const long long q = b >> 1;
+        const int KB = d / 128, J = inter / 256;
+        const int ks = (int)(q % KB);
+        const long long ej = q / KB;
+        const int nb = (int)(ej % J);
+        const long long e = ej / J;
+        // s8t of W2 ([E][d][inter]) as moe_fp4_to_fp8t writes it: [E][inter/128][d/128]
+        const uint32_t v = s8t[(e * (inter / 128) + 2 * nb + h) * KB + ks];
+        const uint32_t w = v * 0x01010101u;
+        reinterpret_cast<uint4 *>(img)[i] = make_uint4(w, w, w, w);
+    }
+    pdl_trigger();
+}
+
+// dy of every pair in expert order, quantised: one warp per pair position.
+// dy = w_tj * dout_t in fp32, then E4M3 with one power-of-two scale per 128
+// channels (the activations' rule); the scale bytes go to the GEMM's per-tile
+// scale layout (row tiles of R pairs, as the forward's plan numbers them).
+__global__ void __launch_bounds__(256) bwd_dy_kernel(const uint16_t *__restrict__ dout, const float *__restrict__ topk_w,
+                                                     const int32_t *__restrict__ topk_idx,
+                                                     const int32_t *__restrict__ sorted_pair,
+                                                     const int32_t *__restrict__ expert_offsets,
+                                                     const int32_t *__restrict__ tile_prefix, uint8_t *__restrict__ dyq,
+                                                     uint8_t *__restrict__ dys_tiles, long long P, int d, int k, int R)
+{
+    pdl_wait();
+    const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (pos >= P) return;
+    const int lane = threadIdx.x & 31;
+    const int p = sorted_pair[pos];
+    const int t = p / k;
+    const int e = topk_idx[p];
+    const float w = topk_w[p];
+    const int local = (int)(pos - expert_offsets[e]);
+    const long long m = tile_prefix[e] + local / R;
+    const int r = local % R;
+    const int G4 = stage_groups(d);
+    const uint4 *src = reinterpret_cast<const uint4 *>(dout + (size_t)t * d);
+    uint8_t *qrow = dyq + (size_t)pos * d;
+    const int n8 = d / 8;
+    for (int c = lane; c - lane < n8; c += 32) {
+        uint4 cur = make_uint4(0, 0, 0, 0);
+        if (c < n8) cur = __ldg(src + c);
+        const uint32_t u[4] = {cur.x, cur.y, cur.z, cur.w};
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            v[2 * i] = w * bf16_bits_to_f32(u[i] & 0xFFFFu);
+            v[2 * i + 1] = w * bf16_bits_to_f32(u[i] >> 16);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (c < n8) {
+            const int ex = e4m3_scale_exp(amax);
+            const float sc = exp2i(-ex);
+            uint2 q;
+            q.x = cvt_e4m3x2(v[0] * sc, v[1] * sc) | (cvt_e4m3x2(v[2] * sc, v[3] * sc) << 16);
+            q.y = cvt_e4m3x2(v[4] * sc, v[5] * sc) | (cvt_e4m3x2(v[6] * sc, v[7] * sc) << 16);
+            reinterpret_cast<uint2 *>(qrow)[c] = q;
+            if ((lane & 15) == 0) {
+                const int grp = c / 16;                      // 128-channel group = K stage of the GEMM
+                dys_tiles[(m * G4 + grp / 4) * kBlockScaleBytes + sf_byte(r, grp % 4)] = (uint8_t)(ex + 127);
+            }
+        }
+    }
+    pdl_trigger();
+}
+
+namespace {
+
+bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
+
+bool bwd_shape_ok(int T, int d, int inter, int E, int k)
+{
+    if (T < 0 || d <= 0 || inter <= 0 || E <= 0 || k <= 0) return false;
+    if (d % 256 || inter % 256) return false;
+    if (k > 8 || k > E || E > 256) return false;
+    if ((long long)T * k >= (1ll << 31)) return false;
+    return true;
+}
+
+// scratch of moe_backward_h: dyq [P][d], its scale tiles, the scale image
+struct BwdLayout {
+    size_t dyq, dys, img, total;
+};
+BwdLayout bwd_layout(int T, int d, int inter, int E, int k)
+{
+    const long long P = (long long)T * k;
+    const int R = gemm_tile_rows(P, E);
+    const size_t tiles = (size_t)max_row_tiles(P, E, R);
+    BwdLayout l;
+    l.dyq = 0;
+    l.dys = round_up256((size_t)P * d);
+    l.img = l.dys + round_up256(tiles * stage_groups(d) * kBlockScaleBytes);
+    l.total = l.img + round_up256((size_t)E * (inter / 128) * (d / 128) * kBlockScaleBytes);
+    return l;
+}
+
+} // namespace
+
+} // namespace fp4moe
+
+using namespace fp4moe;
+
+extern "C" size_t moe_backward_h_workspace_size(int T, int d, int inter, int E, int k)
+{
+    if (!bwd_shape_ok(T, d, inter, E, k)) return 0;
+    return bwd_layout(T, d, inter, E, k).total;
+}
+
+extern "C" moe_status moe_backward_h(const uint16_t *dout, const uint8_t *w2_fp8t, const uint8_t *w2_s8t,
+                                     const float *gu, const void *fwd_workspace, void *workspace,
+                                     size_t workspace_bytes, uint8_t *dgu, uint8_t *dgu_scale, float *dgu_f32, int T,
+                                     int d, int inter, int E, int k, void *stream)
+{
+    if (!dout || !w2_fp8t || !w2_s8t || !gu || !fwd_workspace || !dgu || !dgu_scale) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || d <= 0 || inter <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned_to(dout, 16) || !aligned_to(w2_fp8t, 16) || !aligned_to(gu, 32) || !aligned_to(dgu, 32) ||
+        !aligned_to(fwd_workspace, 256) || (dgu_f32 && !aligned_to(dgu_f32, 32)))
+        return MOE_ERR_INVALID_ARG;
+    if (!bwd_shape_ok(T, d, inter, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const BwdLayout L = bwd_layout(T, d, inter, E, k);
+    if (workspace && (!aligned_to(workspace, 256) || workspace_bytes < L.total)) return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    int num_sms = 0;
+    unsigned *status = nullptr;
+    moe_status st = device_query(&num_sms, &status);
+    if (st != MOE_OK) return st;
+    Workspace fw;
+    if (!workspace_layout(Shapes{T, d, inter, E, k}, &fw)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const uint8_t *fb = static_cast<const uint8_t *>(fwd_workspace);
+    const long long P = (long long)T * k;
+    const int R = gemm_tile_rows(P, E);
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(workspace);
+    bool owned = false;
+    if (!base) {
+        void *p = nullptr;
+        if (cudaMallocAsync(&p, L.total, s) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_WORKSPACE;
+        }
+        base = static_cast<uint8_t *>(p);
+        owned = true;
+    }
+    const int32_t *topk_idx = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_TOPK_IDX]);
+    const float *topk_w = reinterpret_cast<const float *>(fb + fw.off[MOE_WS_TOPK_W]);
+    const int32_t *offs = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_EXPERT_OFFSETS]);
+    const int32_t *sorted_pair = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_SORTED_PAIR]);
+    const int32_t *tile_prefix = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_TILE_PREFIX]);
+    uint8_t *dyq = base + L.dyq, *dys = base + L.dys, *img = base + L.img;
+
+    const long long n16 = (long long)E * (inter / 128) * (d / 128) * (kBlockScaleBytes / 16);
+    cudaError_t e = launch_pdl(bwd_scale_image_kernel, dim3((unsigned)((n16 + 255) / 256)), dim3(256), 0, s, w2_s8t,
+                               img, n16, inter, d);
+    if (e == cudaSuccess)
+        e = launch_pdl(bwd_dy_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, s, dout, topk_w, topk_idx,
+                       sorted_pair, offs, tile_prefix, dyq, dys, P, d, k, R);
+    if (e == cudaSuccess) {
+        GemmArgs g;
+        std::memset(&g, 0, sizeof g);
+        g.tile_rows = R;
+        g.a = dyq;
+        g.a_scale_tiles = dys;
+        g.k = k;
+        g.a_rows = P;
+        g.b = w2_fp8t;
+        g.b_scale = img;
+        g.N = inter;
+        g.K = d;
+        g.expert_offsets = offs;
+        g.tile_prefix = tile_prefix;
+        g.E = E;
+        g.P = P;
+        g.status = status;
+        g.timeout_ns = 2000000000ull;
+        g.num_sms = num_sms;
+        g.gu_in = gu;
+        g.dgu = dgu;
+        g.dgu_scale = dgu_scale;
+        g.dgu_f32 = dgu_f32;
+        e = launch_gemm_dgrad_h(g, inter, s);
+    }
+    if (owned) {
+        cudaError_t f = cudaFreeAsync(base, s);
+        if (e == cudaSuccess) e = f;
+    }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -110,12 +110,19 @@ __host__ __device__ constexpr uint32_t full_arrivals(int) { return 1; }
 // every 8-byte group of 16 codes over a 16-byte slot (codes in the low 8
 // bytes, the high 8 bytes left as they were), but the barrier's transaction
 // count advances by the packed bytes: half the shared-memory footprint.
-constexpr uint32_t B_STAGE_TX = B_STAGE / 2;
+// MODE 3 reads FP8 weights: one byte per code in global and shared memory.
+template <int MODE>
+__host__ __device__ constexpr uint32_t b_stage_tx() { return MODE == 3 ? B_STAGE : B_STAGE / 2; }
 
-// Instruction descriptor of the block-scaled MMA: A = E4M3 (format 0),
-// B = E2M1 (format 5), both K-major, N = 256, M = 128, UE8M0 scales.
-constexpr uint32_t IDESC_BASE = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
-                                ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor of the block-scaled MMA: A = E4M3 (format 0), B =
+// E2M1 (format 5; E4M3 for the backward's FP8 weights, MODE 3), both K-major,
+// N = 256, M = 128, UE8M0 scales.
+template <int MODE>
+__host__ __device__ constexpr uint32_t idesc_base()
+{
+    return (0u << 7) | ((MODE == 3 ? 0u : 5u) << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(BM >> 4) << 24);
+}
 
 
 struct Tile {
@@ -210,7 +217,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
     // of its row tiles waits for that tile's GEMM1 epilogue warps (tile_done)
     // before loading the tile's hq rows, so GEMM2 tiles of early experts run
     // while GEMM1 finishes the last ones.
-    if (MODE == 1) pdl_wait();
+    if (MODE != 2) pdl_wait();
     for (int i = threadIdx.x; i <= E; i += NUM_THREADS) {
         s_offs[i] = g.expert_offsets[i];
         s_tp[i] = g.tile_prefix[i];
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                                               : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
             // A's scales change every fourth stage, and only those stages' copy is
             // read (the MMA thread moves it into tensor memory there)
-            const uint32_t stage_tx = a_tx + B_STAGE_TX + SFB_STAGE;
+            const uint32_t stage_tx = a_tx + b_stage_tx<MODE>() + SFB_STAGE;
             const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
             // GEMM2: the tile's hq rows and scales are complete once every GEMM1
             // epilogue warp that stores them (one per 128-channel block of
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                     if (dense_big) tma_load_2d(sa, &tmA2, fb, ks * BK, ti.row0);
                     for (int b = 0; b < dense_boxes; b++)
                         tma_load_2d(sa + b * kDenseBoxRows * BK, &tmA3, fb, ks * BK, ti.row0 + b * kDenseBoxRows);
-                    if (MODE == 2) {
+                    if (MODE >= 2) {
                         if (small) {
                             for (int b = 0; b < a_boxes; b++)
                                 tma_load_2d(sa + b * A_SMALL_ROWS * BK, &tmA2, fb, ks * BK, ti.row0 + b * A_SMALL_ROWS);
@@ -327,7 +334,10 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                             tma_load_2d(sa, &tmA, fb, ks * BK, ti.row0);
                         }
                     }
-                    tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk + 2 * ks));
+                    if (MODE == 3)   // FP8 weight rows [E * N][K]: the tile's 256 rows at K block ks
+                        tma_load_2d(sb, &tmB, fb, ks * BK, ti.e * g.N + ti.n_block * BN);
+                    else
+                        tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk + 2 * ks));
                     if ((ks & 3) == 0)
                         bulk_copy_g2s(smem + OFF_SFA + stage * SFA_STAGE, a_sf + (ks >> 2) * SFA_STAGE, SFA_STAGE, fb);
                     uint8_t *sfb = smem + OFF_SFB + stage * SFB_STAGE;
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                     for (int kk = 0; kk < BK / 32; kk++) {
                         // A scales: one byte per 128 channels, byte (ks % 4) of the word;
                         // B scales: one byte per 32 K-elements, byte kk of the word
-                        const uint32_t idesc = IDESC_BASE | ((uint32_t)kk << 4) | ((uint32_t)(ks & 3) << 29);
+                        const uint32_t idesc = idesc_base<MODE>() | ((uint32_t)kk << 4) | ((uint32_t)(ks & 3) << 29);
                         tc_mma_mx(tmem + ACC_COL, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa_col, sfb_col,
                                   (ks | kk) != 0);
                     }
@@ -488,6 +498,22 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(acc_empty);
+                if (g.gu_out && r < ti.valid) {
+                    // training: keep g and u (fp32) for the backward's SwiGLU
+                    float *gd = g.gu_out + row * (2 * (size_t)out_dim) + (size_t)ti.n_block * 128 + 64 * half;
+                    float *ud = gd + out_dim;
+#pragma unroll
+                    for (int i = 0; i < 64; i += 8) {
+                        uint32_t wg[8], wu[8];
+#pragma unroll
+                        for (int u = 0; u < 8; u++) {
+                            wg[u] = i < 32 ? g0[i + u] : g1[i - 32 + u];
+                            wu[u] = i < 32 ? u0[i + u] : u1[i - 32 + u];
+                        }
+                        st_global_v8(gd + i, wg);
+                        st_global_v8(ud + i, wu);
+                    }
+                }
                 // SwiGLU with the hardware exp2 and reciprocal approximations
                 // (a few ulp of fp32); h is rounded to E4M3 (3 mantissa bits)
                 // right below, so this error is about 1e-4 of the FP8 step.
@@ -538,6 +564,99 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                     red_release_add(g.tile_done + ti.m_tile, 1);
                     red_release_add(g.all_done, 1);
                 }
+            } else if (MODE == 3) {
+                // Backward (QAT): the accumulator is dh for channels c0 .. c0+127
+                // of the pair (half h of the tile: channels 256 n_block + 128 h).
+                // SwiGLU backward with the forward's g and u:
+                //   dg = dh u s (1 + g (1 - s)),  du = dh g s,  s = 1 / (1 + e^-g);
+                // [dg; du] quantised to E4M3 with one power-of-two scale per 128
+                // channels (the activations' rule).  Pass 0 finds the two amaxes,
+                // pass 1 recomputes and stores; the accumulator is released after.
+                const int I = out_dim;
+                const int c0 = ti.n_block * BN + 128 * half;
+                const bool live = r < ti.valid;
+                const float *grow = g.gu_in + row * (2 * (size_t)I);
+                float amax_g = 0.f, amax_u = 0.f, sg = 1.f, su = 1.f;
+                int eg = 0, eu = 0;
+                for (int pass = 0; pass < 2; pass++) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 4; ch++) {
+                        uint32_t v[32], gv[32], uv[32];
+                        tmem_ld32(trow + 128 * half + 32 * ch, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; q8++) {
+                            uint32_t a[8], b[8];
+                            if (live) {
+                                ld_global_nc_v8(a, grow + c0 + 32 * ch + 8 * q8);
+                                ld_global_nc_v8(b, grow + I + c0 + 32 * ch + 8 * q8);
+                            } else {
+#pragma unroll
+                                for (int u = 0; u < 8; u++) a[u] = b[u] = 0u;
+                            }
+#pragma unroll
+                            for (int u = 0; u < 8; u++) {
+                                gv[8 * q8 + u] = a[u];
+                                uv[8 * q8 + u] = b[u];
+                            }
+                        }
+                        float dg[32], du[32];
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            const float dh = __uint_as_float(v[i]), gg_ = __uint_as_float(gv[i]),
+                                        uu = __uint_as_float(uv[i]);
+                            const float sgm = __fdividef(1.0f, 1.0f + __expf(-gg_));
+                            dg[i] = dh * uu * sgm * (1.0f + gg_ * (1.0f - sgm));
+                            du[i] = dh * gg_ * sgm;
+                        }
+                        if (pass == 0) {
+#pragma unroll
+                            for (int i = 0; i < 32; i++) {
+                                amax_g = fmaxf(amax_g, fabsf(dg[i]));
+                                amax_u = fmaxf(amax_u, fabsf(du[i]));
+                            }
+                        } else if (live) {
+                            uint32_t wg[8], wu[8];
+#pragma unroll
+                            for (int u = 0; u < 8; u++) {
+                                wg[u] = cvt_e4m3x2(dg[4 * u] * sg, dg[4 * u + 1] * sg) |
+                                        (cvt_e4m3x2(dg[4 * u + 2] * sg, dg[4 * u + 3] * sg) << 16);
+                                wu[u] = cvt_e4m3x2(du[4 * u] * su, du[4 * u + 1] * su) |
+                                        (cvt_e4m3x2(du[4 * u + 2] * su, du[4 * u + 3] * su) << 16);
+                            }
+                            uint8_t *qrow = g.dgu + row * (2 * (size_t)I);
+                            st_global_v8(qrow + c0 + 32 * ch, wg);
+                            st_global_v8(qrow + I + c0 + 32 * ch, wu);
+                            if (g.dgu_f32) {
+                                float *frow = g.dgu_f32 + row * (2 * (size_t)I);
+#pragma unroll
+                                for (int q8 = 0; q8 < 4; q8++) {
+                                    uint32_t a[8], b[8];
+#pragma unroll
+                                    for (int u = 0; u < 8; u++) {
+                                        a[u] = __float_as_uint(dg[8 * q8 + u]);
+                                        b[u] = __float_as_uint(du[8 * q8 + u]);
+                                    }
+                                    st_global_v8(frow + c0 + 32 * ch + 8 * q8, a);
+                                    st_global_v8(frow + I + c0 + 32 * ch + 8 * q8, b);
+                                }
+                            }
+                        }
+                    }
+                    if (pass == 0) {
+                        eg = e4m3_scale_exp(amax_g);
+                        eu = e4m3_scale_exp(amax_u);
+                        sg = exp2i(-eg);
+                        su = exp2i(-eu);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+                if (live) {
+                    uint8_t *srow = g.dgu_scale + row * (2 * (size_t)I / 128);
+                    srow[c0 / 128] = (uint8_t)(eg + 127);
+                    srow[(I + c0) / 128] = (uint8_t)(eu + 127);
+                }
             } else {
                 uint32_t v0[32], v1[32], v2[32], v3[32];
                 tmem_ld32(trow + 128 * half, v0);
@@ -570,7 +689,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
         }
     }
 
-    if (MODE == 2) pdl_trigger();
+    if (MODE >= 2) pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -684,6 +803,52 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
     if (!(MODE == 1 && a.a_dense)) ma3 = ma2;   // unused
     return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ma, ma2, ma3, mb, a, out_dim);
+}
+
+// FP8 weight rows [rows][K] (the backward's transposed weights), a 128-byte x
+// 256-row box, 128-byte swizzle
+static bool make_map_fp8_rows(CUtensorMap *m, const uint8_t *b, long long rows, int K)
+{
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {(cuuint32_t)gg::BK, (cuuint32_t)gg::BN};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(b), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm_dgrad_h(const GemmArgs &a, int inter, cudaStream_t st)
+{
+    if (a.P == 0) return cudaSuccess;
+    CUtensorMap ma, ma2, mb;
+    if (!make_map_a(&ma, a.a, a.a_rows, a.K, gg::BM) || !make_map_a(&ma2, a.a, a.a_rows, a.K, gg::A_SMALL_ROWS) ||
+        !make_map_fp8_rows(&mb, a.b, (long long)a.E * a.N, a.K))
+        return cudaErrorInvalidValue;
+    auto kern = gg::grouped_gemm_kernel<3, false, 128>;
+    int smem = gg::Cfg<128>::SMEM_BYTES, threads = gg::Cfg<128>::NUM_THREADS;
+    if (a.tile_rows == 16) {
+        kern = gg::grouped_gemm_kernel<3, false, 16>;
+        smem = gg::Cfg<16>::SMEM_BYTES;
+        threads = gg::Cfg<16>::NUM_THREADS;
+    } else if (a.tile_rows == 32) {
+        kern = gg::grouped_gemm_kernel<3, false, 32>;
+        smem = gg::Cfg<32>::SMEM_BYTES;
+        threads = gg::Cfg<32>::NUM_THREADS;
+    } else if (a.tile_rows == 64) {
+        kern = gg::grouped_gemm_kernel<3, false, 64>;
+        smem = gg::Cfg<64>::SMEM_BYTES;
+        threads = gg::Cfg<64>::NUM_THREADS;
+    } else if (a.tile_rows != 128) {
+        return cudaErrorInvalidValue;
+    }
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * (inter / gg::BN);
+    const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
+    return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ma, ma2, ma2, mb, a, inter);
 }
 
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm<1>(a, inter, st); }

@@ -215,8 +215,21 @@ struct GemmArgs {
     // GEMM2, tests only: wait for a GEMM1 count that never comes (before any
     // copy), so the bounded wait expires
     int stall_test;
+    // GEMM1 (training): g and u of every pair, fp32 [P][2 inter] in expert
+    // order (g at [p][c], u at [p][inter + c]); NULL = not kept
+    float *gu_out;
+    // MODE 3 (backward, dh = W2^T dy and the SwiGLU backward): the forward's
+    // g, u (as gu_out), and the outputs [dg; du] as E4M3 codes [P][2 inter] +
+    // scales [P][2 inter / 128], optionally also fp32 [P][2 inter]
+    const float *gu_in;
+    uint8_t *dgu;
+    uint8_t *dgu_scale;
+    float *dgu_f32;
 };
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st);
 cudaError_t launch_gemm2(const GemmArgs &a, int d, cudaStream_t st);
+// dh = W2^T dy per pair on the FP8 weights (B = [E * inter][d] rows, scales in
+// the tiled scale layout with N = inter, K = d) with the SwiGLU backward fused
+cudaError_t launch_gemm_dgrad_h(const GemmArgs &a, int inter, cudaStream_t st);
 
 } // namespace fp4moe

@@ -59,9 +59,11 @@ def workspace(T: int, d: int, inter: int, E: int, k: int, device="cuda") -> torc
 
 def forward(x: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
             gate_bias: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
-            out: Optional[torch.Tensor] = None, stream=None, routing: bool = False):
+            out: Optional[torch.Tensor] = None, stream=None, routing: bool = False,
+            gu_out: Optional[torch.Tensor] = None):
     """out bf16 [T, d] = MoE layer forward of bf16 x [T, d] (device tensors).
-    With routing=True also returns (topk_idx, topk_w, pair_pos)."""
+    With routing=True also returns (topk_idx, topk_w, pair_pos).  gu_out (fp32
+    [T*k, 2*inter]) keeps GEMM1's g and u for the backward (moe_backward_h)."""
     T, d = x.shape
     if out is None:
         out = torch.empty_like(x)
@@ -72,7 +74,7 @@ def forward(x: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
         pp = torch.empty((T * k,), dtype=torch.int32, device=x.device)
     capi.moe_forward_ex(x, gate_w, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, out, k,
                         stream=stream, gate_bias=gate_bias, workspace=ws,
-                        topk_idx_out=ti, topk_w_out=tw, pair_pos_out=pp)
+                        topk_idx_out=ti, topk_w_out=tw, pair_pos_out=pp, gu_out=gu_out)
     if routing:
         return out, ti, tw, pp
     return out

@@ -222,6 +222,11 @@ typedef struct moe_forward_opts {
                                   cudaEvent_t, recorded on the stream before the
                                   first stage, between stages and after the last
                                   (per-stage timing); NULL = none */
+    float *gu_out;             /* optional (training): device fp32 [T*k][2*inter], 32-byte
+                                  aligned: g and u of every pair in expert order (row
+                                  workspace pair position, g at [p][c], u at [p][inter + c]),
+                                  the tensor-core fp32 sums GEMM1 applies SwiGLU to; the
+                                  input moe_backward_h needs.  NULL = not kept */
 } moe_forward_opts;
 
 /* Test only (failure detection without a GPU fault): GEMM2 waits for a
@@ -252,6 +257,42 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w,
                           const uint8_t *w2_fp4, const uint8_t *w2_scale,
                           uint16_t *out, int T, int d, int inter, int E, int k,
                           void *stream, const moe_forward_opts *opts);
+
+/*
+ * moe_backward_h -- the first GEMM of the layer's backward pass in FP4
+ * quantisation-aware training, with the SwiGLU backward fused (first page,
+ * section 4: the backward computes with the FP8 weights the FP4 weights
+ * dequantise to -- moe_fp4_to_fp8t -- and transposed 128 x 128 blocks are not
+ * re-quantised; section 3.2: fixed summation order, no atomics).  For every
+ * token-expert pair p = t*k + j routed to expert e, in the forward's expert
+ * order (pair position pos = pair_pos[p]):
+ *   dy     = topk_w[t][j] * dout[t]                       fp32
+ *   dyq    = E4M3 of dy, one power-of-two scale per 128 channels (the rule of
+ *            moe_quantize_act)
+ *   dh     = W2[e]^T dyq                                  block-scaled FP8 MMA, fp32
+ *   dg     = dh * u * s * (1 + g * (1 - s)),  du = dh * g * s,  s = 1 / (1 + e^-g)
+ *            (g, u: the forward's, from moe_forward_opts.gu_out)
+ *   [dg; du] -> E4M3 codes with one power-of-two scale per 128 channels
+ *   dout           device, bf16 [T][d]: the gradient at the layer output
+ *   w2_fp8t        device, moe_fp4_to_fp8t output for W2 ([E][d][inter]): E4M3
+ *                  [E][inter][d], 16-byte aligned
+ *   w2_s8t         device, its block exponents [E][inter/128][d/128]
+ *   gu             device, fp32 [T*k][2*inter] (moe_forward_opts.gu_out)
+ *   fwd_workspace  device, the workspace of the forward call that produced gu
+ *                  (its routing and dispatch-plan regions are read)
+ *   workspace      device scratch of moe_backward_h_workspace_size bytes,
+ *                  256-byte aligned, or NULL (then allocated stream-ordered)
+ *   dgu            device, E4M3 codes [T*k][2*inter] in expert order, 32-byte aligned:
+ *                  dg at [pos][c], du at [pos][inter + c]
+ *   dgu_scale      device, [T*k][2*inter/128]: byte e + 127 of each 128 channels
+ *   dgu_f32        device, fp32 [T*k][2*inter] (the unquantised dg, du), or NULL
+ * Requires d % 256 == 0 and inter % 256 == 0, 1 <= k <= 8, k <= E <= 256.
+ * Argument errors are reported before anything is enqueued.
+ */
+size_t moe_backward_h_workspace_size(int T, int d, int inter, int E, int k);
+moe_status moe_backward_h(const uint16_t *dout, const uint8_t *w2_fp8t, const uint8_t *w2_s8t, const float *gu,
+                          const void *fwd_workspace, void *workspace, size_t workspace_bytes, uint8_t *dgu,
+                          uint8_t *dgu_scale, float *dgu_f32, int T, int d, int inter, int E, int k, void *stream);
 
 /* Bytes of workspace moe_forward_ex needs for these shapes (0 for bad shapes). */
 size_t moe_workspace_size(int T, int d, int inter, int E, int k);

@@ -59,6 +59,36 @@ def q8(v):
     return out
 
 
+def pair_dgu(g, u, dy, W2e, quantize_grads=True):
+    """The first half of one token-expert pair's backward, from the gradient
+    at y: dh = W2^T dy (on the FP8 weights), then the SwiGLU backward
+    dg = dh u sig(g) (1 + g (1 - sig(g))), du = dh g sig(g).  g, u are the
+    forward's (rounded to fp32), dy the pair's gradient at y (w_j dout).
+    Returns (dyq, dg, du, dgu): dy as the GEMM reads it (E4M3 per 128 channels
+    with quantize_grads), dg and du unquantised, and [dg; du] as the next
+    GEMM reads it (E4M3 per 128 channels with quantize_grads)."""
+    if quantize_grads:
+        dy = q8(dy)
+    dh = W2e.T @ dy
+    sig = 1.0 / (1.0 + np.exp(-g))
+    dg = dh * u * sig * (1.0 + g * (1.0 - sig))
+    du = dh * g * sig
+    dgu = np.concatenate([dg, du])
+    if quantize_grads:
+        dgu = q8(dgu)
+    return dy, dg, du, dgu
+
+
+def forward_gu(xq_row, xs_row, e, w13_fp4, w13_scale):
+    """g and u of a pair as the forward computes them: exact sums rounded to fp32."""
+    xd = _E4M3[xq_row] * np.ldexp(1.0, np.repeat(np.asarray(xs_row, np.int64) - 127, 128))
+    W13f = fp4_weights(w13_fp4[e:e + 1], w13_scale[e:e + 1])[0]
+    inter = W13f.shape[0] // 2
+    g = (W13f[:inter] @ xd).astype(np.float32).astype(np.float64)
+    u = (W13f[inter:] @ xd).astype(np.float32).astype(np.float64)
+    return g, u
+
+
 def qat_backward(x, topk_idx, topk_w, w13_fp4, w13_scale, w2_fp4, w2_scale, dout, quantize_grads=True):
     """Gradients of the layer output's inner product with `dout` (bf16 bits
     [T, d]) for the forward of x (bf16 bits [T, d]) under the given routing.
@@ -92,15 +122,7 @@ def qat_backward(x, topk_idx, topk_w, w13_fp4, w13_scale, w2_fp4, w2_scale, dout
             hd = _E4M3[hq] * np.ldexp(1.0, np.repeat(hs.astype(np.int64) - 127, 128))
             dy = float(topk_w[t, j]) * do[t]
             dw[t, j] = do[t] @ yf
-            if quantize_grads:
-                dy = q8(dy)
-            dh = W2[e].T @ dy
-            sig = 1.0 / (1.0 + np.exp(-g))
-            dg = dh * u * sig * (1.0 + g * (1.0 - sig))
-            du = dh * g * sig
-            dgu = np.concatenate([dg, du])
-            if quantize_grads:
-                dgu = q8(dgu)
+            dy, _, _, dgu = pair_dgu(g, u, dy, W2[e], quantize_grads)
             dx[t] += W13[e].T @ dgu
             dW2[e] += np.outer(dy, hd)
             dW13[e] += np.outer(dgu, xd[t])

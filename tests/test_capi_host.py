@@ -133,3 +133,17 @@ def test_workspace_layout(capi):
             assert end <= nxt
         assert st[capi.MOE_WS_XS] == xs and st[capi.MOE_WS_HS_TILES] == gh * 512 and st[capi.MOE_WS_Y] == 2 * d
     assert capi.moe_workspace_size(8, 384, 128, 8, 2) == 0
+
+
+def test_backward_h_argument_checks(capi):
+    """moe_backward_h rejects bad shapes and pointers before touching CUDA."""
+    lib = capi.lib()
+    F = FAKE
+    assert lib.moe_backward_h(F, F, F, F, F, None, 0, F, F, None, 8, 256, 384, 8, 2, None) == 2   # inter % 256
+    assert lib.moe_backward_h(F, F, F, F, F, None, 0, F, F, None, 8, 384, 256, 8, 2, None) == 2   # d % 256
+    assert lib.moe_backward_h(F, F, F, F, F, None, 0, None, F, None, 8, 256, 256, 8, 2, None) == 1  # no output
+    assert lib.moe_backward_h(F, F, F, F + 16, F, None, 0, F, F, None, 8, 256, 256, 8, 2, None) == 1  # gu alignment
+    assert lib.moe_backward_h(F, F, F, F, F, F, 16, F, F, None, 8, 256, 256, 8, 2, None) == 4      # workspace too small
+    assert lib.moe_backward_h(F, F, F, F, F, None, 0, F, F, None, 0, 256, 256, 8, 2, None) == 0    # T == 0: no-op
+    assert capi.moe_backward_h_workspace_size(8, 256, 384, 8, 2) == 0
+    assert capi.moe_backward_h_workspace_size(8, 256, 256, 8, 2) > 0
