@@ -76,7 +76,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool layer_shape_ok(int T, int d, int inter, int E, int k)
 {
     if (T < 0 || d <= 0 || inter <= 0 || E <= 0 || k <= 0) return false;
-    if (d % 256 || inter % 128) return false;
+    if (d % 128 || inter % 128) return false;
     if (k > 8 || k > E || E > 256) return false;
     if ((long long)T * k >= (1ll << 31)) return false;
     return true;
@@ -165,7 +165,7 @@ moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E,
     if (!w || !w_fp4 || !w_scale) return MOE_ERR_INVALID_ARG;
     if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
     if (!aligned(w, 16) || !aligned(w_fp4, 16) || !aligned(w_scale, 16)) return MOE_ERR_INVALID_ARG;
-    if (K % 128 || N % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (K % 128 || N % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((long long)E * N * K == 0) return MOE_OK;
     DeviceInfo *di;
     moe_status st = device_info(&di);
@@ -179,7 +179,7 @@ moe_status moe_fp4_to_fp8t(const uint8_t *w_fp4, const uint8_t *w_scale, uint8_t
     if (!w_fp4 || !w_scale || !w8t || !s8t) return MOE_ERR_INVALID_ARG;
     if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
     if (!aligned(w_fp4, 16) || !aligned(w_scale, 16) || !aligned(w8t, 16)) return MOE_ERR_INVALID_ARG;
-    if (K % 128 || N % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (K % 128 || N % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((long long)E * N * K == 0) return MOE_OK;
     if ((long long)E * (N / 128) * (K / 128) > 0x7FFFFFFFLL) return MOE_ERR_UNSUPPORTED_SHAPE;
     DeviceInfo *di;
@@ -222,7 +222,10 @@ moe_status moe_route(const uint16_t *x, const float *gate_w, const float *gate_b
                  wpb = round_up((size_t)E * d * 2, 256), wnb = round_up((size_t)E * 4, 256);
     const size_t bytes = zb + (tc ? wtb + 2 * wpb + wnb + (size_t)T * 4 : 0);
     void *z = nullptr;
-    if (cudaMallocAsync(&z, bytes, s) != cudaSuccess) return MOE_ERR_WORKSPACE;
+    if (cudaMallocAsync(&z, bytes, s) != cudaSuccess) {
+        cudaGetLastError();                      // nothing was enqueued; leave no error behind
+        return MOE_ERR_WORKSPACE;
+    }
     cudaError_t e;
     if (tc) {
         uint8_t *b = static_cast<uint8_t *>(z);
@@ -261,7 +264,10 @@ moe_status moe_dispatch_plan(const int32_t *topk_idx, int32_t *expert_offsets, i
     cudaStream_t s = (cudaStream_t)stream;
     const size_t scratch = plan_scratch_bytes((long long)T * k, E);
     void *counts = nullptr;
-    if (scratch && cudaMallocAsync(&counts, scratch, s) != cudaSuccess) return MOE_ERR_WORKSPACE;
+    if (scratch && cudaMallocAsync(&counts, scratch, s) != cudaSuccess) {
+        cudaGetLastError();                      // nothing was enqueued; leave no error behind
+        return MOE_ERR_WORKSPACE;
+    }
     cudaError_t e = launch_plan(topk_idx, expert_offsets, sorted_pair, pair_pos, nullptr, (int *)counts, T, E, k,
                                 di->status, s);
     cudaError_t f = counts ? cudaFreeAsync(counts, s) : cudaSuccess;
@@ -315,7 +321,10 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     bool owned = false;
     if (!base) {
         void *p = nullptr;
-        if (cudaMallocAsync(&p, ws.total, s) != cudaSuccess) return MOE_ERR_WORKSPACE;
+        if (cudaMallocAsync(&p, ws.total, s) != cudaSuccess) {
+            cudaGetLastError();                  // nothing was enqueued; leave no error behind
+            return MOE_ERR_WORKSPACE;
+        }
         base = static_cast<uint8_t *>(p);
         owned = true;
     }

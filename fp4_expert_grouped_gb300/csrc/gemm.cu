@@ -229,7 +229,9 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
     if (MODE == 1) pdl_trigger();
     const uint32_t tmem = *tmem_holder;
 
-    const int nb = (MODE == 1) ? out_dim / 128 : out_dim / BN;
+    // GEMM2: one tile per pair of W2's 128-row blocks (the last alone when
+    // d / 128 is odd)
+    const int nb = (MODE == 1) ? out_dim / 128 : MODE == 2 ? weight_pairs(out_dim) : out_dim / BN;
     const long long total_tiles = (long long)s_tp[E] * nb;
     const int nk = g.K / BK;
     const uint64_t tmo = g.timeout_ns;
@@ -257,6 +259,13 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
             // and [d/2 + 128 t, +128)) are adjacent blocks of the tiled layout,
             // pair t: blocks blk + 2 ks and blk + 2 ks + 1.
             const long long blk = weight_block(ti.e, ti.n_block, 0, g.N, g.K);
+            // a pair of one row block: its K blocks are consecutive, and only
+            // its 512 bytes of scales are fetched (the box's second block is
+            // whatever follows, or zeros past the end, and feeds discarded
+            // accumulator columns)
+            const bool single = MODE == 2 && weight_pair_single(ti.n_block, g.N);
+            const int bstride = single ? 1 : 2;
+            const uint32_t sfb_bytes = single ? kBlockScaleBytes : 2 * kBlockScaleBytes;
             const bool small = TR <= 64 || ti.valid <= SMALL_TILE_ROWS;   // 16/32/64-row tiles: always 16-row boxes
             const int a_boxes = small ? (ti.valid + A_SMALL_ROWS - 1) / A_SMALL_ROWS : 1;
             // GEMM1: a dense tile reads its rows from the expert-ordered copy, a
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                                               : (small ? a_boxes * A_SMALL_ROWS * BK : A_STAGE);
             // A's scales change every fourth stage, and only those stages' copy is
             // read (the MMA thread moves it into tensor memory there)
-            const uint32_t stage_tx = a_tx + b_stage_tx<MODE>() + SFB_STAGE;
+            const uint32_t stage_tx = a_tx + b_stage_tx<MODE>() + sfb_bytes;
             const uint8_t *a_sf = g.a_scale_tiles + (size_t)ti.m_tile * ga * SFA_STAGE;
             // GEMM2: the tile's hq rows and scales are complete once every GEMM1
             // epilogue warp that stores them (one per 128-channel block of
@@ -337,11 +346,11 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                     if (MODE == 3)   // FP8 weight rows [E * N][K]: the tile's 256 rows at K block ks
                         tma_load_2d(sb, &tmB, fb, ks * BK, ti.e * g.N + ti.n_block * BN);
                     else
-                        tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk + 2 * ks));
+                        tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk + bstride * ks));
                     if ((ks & 3) == 0)
                         bulk_copy_g2s(smem + OFF_SFA + stage * SFA_STAGE, a_sf + (ks >> 2) * SFA_STAGE, SFA_STAGE, fb);
                     uint8_t *sfb = smem + OFF_SFB + stage * SFB_STAGE;
-                    bulk_copy_g2s(sfb, g.b_scale + (blk + 2 * ks) * kBlockScaleBytes, 2 * kBlockScaleBytes, fb);
+                    bulk_copy_g2s(sfb, g.b_scale + (blk + bstride * ks) * kBlockScaleBytes, sfb_bytes, fb);
                 }
                 if (MODE == 1) {
                     __syncwarp();   // the stage's expect_tx is armed before any gather lands
@@ -666,10 +675,12 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(acc_empty);
-                if (r < ti.valid) {
-                    // accumulator half h holds output columns of weight block
-                    // n_block + h * d/256 (the tile's pair of blocks)
-                    uint16_t *dst = g.y + row * out_dim + (size_t)(ti.n_block + half * (out_dim / 256)) * 128;
+                // accumulator half h holds output columns of weight block
+                // n_block + h * ceil(d/256) (the tile's pair of blocks; none for
+                // half 1 of a pair of one block)
+                const int ob = ti.n_block + half * weight_pairs(out_dim);
+                if (r < ti.valid && ob < out_dim / 128) {
+                    uint16_t *dst = g.y + row * out_dim + (size_t)ob * 128;
 #pragma unroll
                     for (int c = 0; c < 4; c++) {
                         const uint32_t *v = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
@@ -798,7 +809,7 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
     }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    const int nb = (MODE == 1) ? out_dim / 128 : out_dim / gg::BN;
+    const int nb = (MODE == 1) ? out_dim / 128 : weight_pairs(out_dim);
     const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * nb;
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
     if (!(MODE == 1 && a.a_dense)) ma3 = ma2;   // unused

@@ -21,12 +21,17 @@ constexpr int kTileN = 256;   // weight rows per tile = MMA N
 constexpr int kTileK = 128;   // K per pipeline stage
 
 // Tiled MXFP4 weight layout written by moe_pack_fp4 (see fp4moe.h): the
-// matrix [N][K] of an expert is cut into 128 x 128 blocks.  The 128-row block
-// n/128 = h * N/256 + j (half h of N, pair j) at K block k/128 is block
-//   b = ((e * N/256 + j) * K/128 + k/128) * 2 + h,
-// so the two blocks a GEMM tile multiplies in one stage -- a 128-row block and
-// its partner N/2 rows further (W13: the gate rows and the up rows of the same
-// channels) -- are adjacent: one TMA box and one scale copy fetch both.
+// matrix [N][K] of an expert is cut into 128 x 128 blocks, NB = N/128 rows of
+// them.  The row blocks form pairs: with H = ceil(NB/2), row block n128 is
+// half h = (n128 >= H) of pair j = n128 - h * H, i.e. pair j holds row blocks
+// j and j + H (for W13 the gate and up rows of the same channels; for W2
+// output rows [128 j, +128) and [128 (j + H), +128)).  At K block k128 the two
+// blocks of pair j are neighbours:
+//   b = e * NB * K/128 + (j * K/128 + k128) * 2 + h          (j < NB/2),
+// so a GEMM tile fetches both with one TMA box and one scale copy.  When NB
+// is odd, the last pair (j = NB/2) holds row block j alone, its K blocks
+// consecutive after the others:
+//   b = e * NB * K/128 + 2 * (NB/2) * K/128 + k128.
 // Block b holds
 //   codes:  8192 bytes at b * 8192, row r (0..127) at r * 64, two codes per
 //           byte, low nibble = even k
@@ -35,10 +40,17 @@ constexpr int kTileK = 128;   // K per pipeline stage
 //           order the tensor-core scale-factor copy reads.
 constexpr int kBlockCodeBytes = 128 * 64;
 constexpr int kBlockScaleBytes = 512;
+// pairs of row blocks (GEMM tiles of 256 weight rows) of an N-row matrix
+__host__ __device__ inline int weight_pairs(int N) { return (N / 128 + 1) / 2; }
+// whether pair j of an N-row matrix holds a single row block
+__host__ __device__ inline bool weight_pair_single(int j, int N) { return (N / 128) % 2 == 1 && j == (N / 128) / 2; }
 __host__ __device__ inline long long weight_block(long long e, int n128, int k128, int N, int K)
 {
-    const int J = N / 256;
-    return ((e * J + n128 % J) * (K / 128) + k128) * 2 + n128 / J;
+    const int NB = N / 128, KB = K / 128, H = (NB + 1) / 2;
+    const int h = n128 >= H ? 1 : 0;
+    const int j = n128 - h * H;
+    const long long base = e * NB * KB;
+    return j < NB / 2 ? base + ((long long)j * KB + k128) * 2 + h : base + 2LL * (NB / 2) * KB + k128;
 }
 __host__ __device__ inline int sf_byte(int r, int j) { return (r % 32) * 16 + (r / 32) * 4 + j; }
 
@@ -107,9 +119,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // ---- launchers (kernels.cu) ----------------------------------------------
-// rows = E * N; writes the tiled layout above (N % 256 == 0, K % 128 == 0)
+// rows = E * N; writes the tiled layout above (N % 128 == 0, K % 128 == 0)
 cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, int E, int N, int K, cudaStream_t st);
-// FP8 weights for the backward pass, transposed (N % 256 == 0, K % 128 == 0):
+// FP8 weights for the backward pass, transposed (N % 128 == 0, K % 128 == 0):
 // w8t [E][K][N] E4M3 codes, s8t [E][K/128][N/128] block exponents + 127
 cudaError_t launch_fp4_to_fp8t(const uint8_t *w_fp4, const uint8_t *w_scale, uint8_t *w8t, uint8_t *s8t, int E, int N,
                                int K, cudaStream_t st);

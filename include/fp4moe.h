@@ -31,9 +31,9 @@
  *  - Return value: MOE_OK or an error code; nothing throws across the ABI.
  *    Asynchronous device errors surface as MOE_ERR_CUDA from a later call, or
  *    through moe_get_device_status.
- *  - Shapes: T >= 0 (T == 0 is a no-op that returns MOE_OK), d % 256 == 0
- *    (d % 128 == 0 for moe_quantize_act / moe_route), inter % 128 == 0,
- *    1 <= k <= 8, k <= E <= 256, T * k < 2^31.
+ *  - Shapes: T >= 0 (T == 0 is a no-op that returns MOE_OK), d % 128 == 0,
+ *    inter % 128 == 0, 1 <= k <= 8, k <= E <= 256, T * k < 2^31
+ *    (moe_backward_h: d % 256 == 0, inter % 256 == 0).
  *  - Alignment: every device pointer 16-byte aligned; packed weights 32-byte
  *    aligned (the tensor-memory-access rule for packed 4-bit data).
  *  - Results are deterministic: repeated calls give identical bits, and a
@@ -74,11 +74,14 @@ int moe_version(void);
  *            (X = -127 for an all-zero block), clamped to [-127, 127]; codes
  *            are the round-to-nearest-even E2M1 of w * 2^-X saturated to +-6,
  *            the scale is the UE8M0 byte X + 127.
- *   layout   each expert's [N][K] matrix is cut into 128 x 128 blocks; the
- *            128-row block n/128 = h * N/256 + j (half h of N, pair j) at K
- *            block k/128 is block b = ((e * N/256 + j) * K/128 + k/128) * 2 + h,
- *            so a 128-row block and its partner N/2 rows further (for W13 the
- *            gate and up rows of the same channels) are adjacent:
+ *   layout   each expert's [N][K] matrix is cut into 128 x 128 blocks, NB = N/128
+ *            rows and KB = K/128 columns of them.  With H = ceil(NB/2), row
+ *            block n/128 is half h = (n/128 >= H) of pair j = n/128 - h * H; at
+ *            K block k/128 the two blocks of pair j are adjacent:
+ *              b = e * NB * KB + (j * KB + k/128) * 2 + h        (j < NB/2)
+ *            (for W13 the gate and up rows of the same channels).  When NB is
+ *            odd the last row block (j = NB/2) stands alone, its K blocks
+ *            consecutive: b = e * NB * KB + 2 * (NB/2) * KB + k/128.  Then:
  *   w_fp4    device, E*N*K/2 bytes: block b at b * 8192, its row n % 128 at
  *            (n % 128) * 64, two codes per byte, the low nibble holding the
  *            even k (so one block is 8 KB of contiguous memory)
@@ -88,7 +91,7 @@ int moe_version(void);
  *            scale-factor copy reads, so the forward loads it with one copy)
  * For the layer: W13 is [E][2*inter][d] (rows 0..inter-1 = gate projection,
  * inter..2*inter-1 = up projection), W2 is [E][d][inter].
- * Requires N % 256 == 0, K % 128 == 0.  Load-time operation, off the hot path.
+ * Requires N % 128 == 0, K % 128 == 0.  Load-time operation, off the hot path.
  */
 moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale,
                         int E, int N, int K, void *stream);
@@ -108,7 +111,7 @@ moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale,
  *                   (e * K + k) * N + n (transposed, N contiguous), 16-byte aligned
  *   s8t             device, E*(K/128)*(N/128) bytes: B + 127 of block (bn, bk)
  *                   at (e * K/128 + bk) * N/128 + bn
- * Requires N % 256 == 0, K % 128 == 0.  Argument errors are reported before
+ * Requires N % 128 == 0, K % 128 == 0.  Argument errors are reported before
  * any launch; the outputs are written on the stream.  Load-time operation
  * (once per weight update), off the forward's hot path.
  */

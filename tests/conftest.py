@@ -31,22 +31,51 @@ def read_golden(name):
 # A pure permutation of the plain layout the oracle writes ([E][N][K/2] codes,
 # [E][N][K/32] scales), used to compare the two bit for bit.
 
+def weight_block(e, n128, k128, N, K):
+    """Block number of 128 x 128 block (n128, k128) of expert e in the tiled
+    layout: row blocks pair as (j, j + H), H = ceil(NB/2), NB = N/128; a pair's
+    two blocks are neighbours at each K block; with NB odd the last row block
+    is alone, its K blocks consecutive after the pairs'."""
+    NB, KB = N // 128, K // 128
+    H = (NB + 1) // 2
+    h = 1 if n128 >= H else 0
+    j = n128 - h * H
+    base = e * NB * KB
+    return base + (j * KB + k128) * 2 + h if j < NB // 2 else base + 2 * (NB // 2) * KB + k128
+
+
 def tile_codes(fp4):
-    """plain codes [E][N][K/2] -> tiled bytes [E][N/256 pairs j][K/128][2 halves h][128 rows][64]:
-    the 128-row block h * N/256 + j goes to block ((e * N/256 + j) * K/128 + k/128) * 2 + h."""
+    """plain codes [E][N][K/2] -> tiled bytes [E * NB * KB blocks][128 rows][64]."""
     import numpy as np
     E, N, K2 = fp4.shape
-    a = fp4.reshape(E, 2, N // 256, 128, K2 // 64, 64)            # (e, h, j, r, kb, byte)
-    return np.ascontiguousarray(a.transpose(0, 2, 4, 1, 3, 5))
+    K = 2 * K2
+    NB, KB = N // 128, K // 128
+    out = np.empty((E * NB * KB, 128, 64), np.uint8)
+    for n128 in range(NB):
+        for kb in range(KB):
+            idx = [weight_block(e, n128, kb, N, K) for e in range(E)]
+            out[idx] = fp4[:, n128 * 128:(n128 + 1) * 128, kb * 64:(kb + 1) * 64]
+    return out
 
 
 def tile_scales(sc):
-    """plain scales [E][N][K/32] -> tiled bytes [E][N/256][K/128][2][512] in the block
+    """plain scales [E][N][K/32] -> tiled bytes [E * NB * KB blocks][512] in the block
     order of tile_codes, the byte of row r and sub-block j at (r % 32) * 16 + (r / 32) * 4 + j."""
     import numpy as np
     E, N, K32 = sc.shape
-    a = sc.reshape(E, 2, N // 256, 4, 32, K32 // 4, 4)       # (e, h, pair, r/32, r%32, kt, j)
-    return np.ascontiguousarray(a.transpose(0, 2, 5, 1, 4, 3, 6)).reshape(E, N // 256, K32 // 4, 2, 512)
+    K = 32 * K32
+    NB, KB = N // 128, K // 128
+    out = np.empty((E * NB * KB, 512), np.uint8)
+    r = np.arange(128)
+    for n128 in range(NB):
+        for kb in range(KB):
+            idx = [weight_block(e, n128, kb, N, K) for e in range(E)]
+            blk = sc[:, n128 * 128:(n128 + 1) * 128, kb * 4:(kb + 1) * 4]       # [E][128][4]
+            img = np.empty((E, 512), np.uint8)
+            for j in range(4):
+                img[:, (r % 32) * 16 + (r // 32) * 4 + j] = blk[:, :, j]
+            out[idx] = img
+    return out
 
 
 def sf_byte(r, j):

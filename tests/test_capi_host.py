@@ -62,7 +62,7 @@ def test_forward_argument_checks(capi):
     assert fwd(lib, x=FAKE + 2) == INV                      # misaligned activations
     assert fwd(lib, w13=FAKE + 16) == INV                   # packed weights need 32-byte alignment
     assert fwd(lib, T=-1) == INV
-    assert fwd(lib, d=384) == SHAPE                         # d % 256
+    assert fwd(lib, d=320) == SHAPE                         # d % 128
     assert fwd(lib, inter=192) == SHAPE                     # inter % 128
     assert fwd(lib, k=9, E=16) == SHAPE
     assert fwd(lib, k=4, E=3) == SHAPE
@@ -86,8 +86,8 @@ def test_other_entry_points_reject_bad_arguments(capi):
     lib = capi.lib()
     assert lib.moe_pack_fp4(None, FAKE, FAKE, 1, 128, 128, None) == 1
     assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 128, 96, None) == 2     # K % 128
-    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 64, 128, None) == 2     # N % 256
-    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 384, 128, None) == 2
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 64, 128, None) == 2     # N % 128
+    assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 1, 320, 128, None) == 2
     assert lib.moe_pack_fp4(FAKE, FAKE, FAKE, 0, 256, 128, None) == 0
     assert lib.moe_quantize_act(FAKE, FAKE, FAKE, 4, 100, None) == 2
     assert lib.moe_quantize_act(FAKE, FAKE, FAKE, 0, 128, None) == 0
@@ -103,7 +103,7 @@ def test_fp4_to_fp8t_argument_checks(capi):
     assert lib.moe_fp4_to_fp8t(None, FAKE, FAKE, FAKE, 1, 256, 128, None) == 1
     assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE + 8, FAKE, 1, 256, 128, None) == 1     # w8t not 16-byte aligned
     assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, -1, 256, 128, None) == 1
-    assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, 1, 128, 128, None) == 2          # N % 256
+    assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, 1, 192, 128, None) == 2          # N % 128
     assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, 1, 256, 96, None) == 2           # K % 128
     assert lib.moe_fp4_to_fp8t(FAKE, FAKE, FAKE, FAKE, 0, 256, 128, None) == 0          # nothing to do
 
@@ -132,7 +132,8 @@ def test_workspace_layout(capi):
             nxt = off[i + 1] if i + 1 < capi.MOE_WS_COUNT else total
             assert end <= nxt
         assert st[capi.MOE_WS_XS] == xs and st[capi.MOE_WS_HS_TILES] == gh * 512 and st[capi.MOE_WS_Y] == 2 * d
-    assert capi.moe_workspace_size(8, 384, 128, 8, 2) == 0
+    assert capi.moe_workspace_size(8, 320, 128, 8, 2) == 0
+    assert capi.moe_workspace_size(8, 384, 128, 8, 2) > 0                     # d % 128 is enough
 
 
 def test_backward_h_argument_checks(capi):

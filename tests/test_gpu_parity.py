@@ -118,6 +118,20 @@ def test_pack_fp4_bitexact_special_values():
     assert_packs_equal(fp4, sc, of, os_)
 
 
+@pytest.mark.parametrize("E,N,K", [(2, 384, 256), (3, 640, 384), (1, 128, 128)])
+def test_pack_fp4_bitexact_odd_row_blocks(E, N, K):
+    """N / 128 odd (d % 256 == 128 for W2): the last row block of each expert
+    is stored alone in the tiled layout; the packs equal the oracle's after the
+    layout's permutation."""
+    rng = np.random.default_rng(E * N + K)
+    w = (rng.normal(0, 1, (E, N, K)) / np.sqrt(K)).astype(np.float32)
+    fp4 = torch.empty((E, N, K // 2), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((E, N, K // 32), dtype=torch.uint8, device=DEV)
+    capi().moe_pack_fp4(torch.from_numpy(w).to(DEV), fp4, sc)
+    of, os_ = oracle.pack_fp4(w)
+    assert_packs_equal(fp4, sc, of, os_)
+
+
 def test_quantize_act_bitexact():
     rng = np.random.default_rng(101)
     T, d = 37, 768
@@ -245,12 +259,48 @@ def test_forward_tiny_all_tokens():
     (150, 256, 128, 16, 2, True),        # 32-row tiles with the copy, ragged tails and empty experts
     (90, 512, 128, 8, 2, False),         # 64-row tiles: one or two 32-row boxes of the copy per stage
     (120, 256, 256, 8, 2, True),         # 64-row tiles, biased: experts over 64 pairs, empty experts
+    (40, 384, 128, 8, 2, False),         # d % 256 == 128: W2's last row block alone (GEMM2 tile of one block)
+    (300, 640, 256, 16, 4, True),        # d = 5 blocks, 128-row tiles with the expert-ordered copy
+    (1100, 1152, 128, 64, 4, True),      # d = 9 blocks, the tensor-core gate, odd K blocks in GEMM1
 ])
 def test_forward_small_shapes(T, d, inter, E, k, bias):
     w, x, gw, b, w13, w2 = small_case(T, d, inter, E, k, seed=T + d, bias=bias)
     if bias:
         b = torch.from_numpy(np.random.default_rng(T).normal(0, 1, E).astype(np.float32))
     run_small_forward(w, x, gw, b, w13, w2)
+
+
+def test_moe_forward_itself_with_its_own_workspace():
+    """The layer through the exact moe_forward symbol (the library allocates
+    and frees its workspace on the stream), against the oracle."""
+    w, x, gw, b, w13, w2 = small_case(200, 512, 256, 16, 4, seed=404)
+    pk = layer().pack_experts(w13.to(DEV), w2.to(DEV))
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=DEV)
+    capi().moe_forward(x.to(DEV), gw.to(DEV), pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, out, w.k)
+    assert capi().moe_get_device_status() == 0
+    f13, s13 = oracle.pack_fp4(w13.numpy())
+    f2, s2 = oracle.pack_fp4(w2.numpy())
+    ref, _, _ = oracle.moe_forward(inputs.bf16_bits(x), gw.numpy(), f13, s13, f2, s2, w.k)
+    check_layer_tolerance(inputs.bf16_bits(out), ref)
+    again = layer().forward(x.to(DEV), gw.to(DEV), pk, w.k)           # caller workspace: the same bits
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+
+
+def test_moe_forward_workspace_allocation_failure_enqueues_nothing():
+    """A workspace the device cannot hold: moe_forward's stream-ordered
+    allocation fails and the call returns MOE_ERR_WORKSPACE before anything is
+    enqueued (the pointers are never touched: they are not even valid); the
+    stream stays idle, no error is left behind, and the next call works."""
+    c = capi()
+    T, d, inter, E, k = 1 << 26, 512, 128, 8, 8            # workspace ~600 GB: y alone is T*k*d*2 bytes
+    assert c.moe_workspace_size(T, d, inter, E, k) > 400 * (1 << 30)
+    fake = 0x100000
+    s = torch.cuda.Stream()
+    rc = c.lib().moe_forward(fake, fake, fake, fake, fake, fake, fake, T, d, inter, E, k, s.cuda_stream)
+    assert rc == 4                                          # MOE_ERR_WORKSPACE
+    assert s.query()                                        # nothing was enqueued
+    assert c.moe_get_device_status(s) == 0
+    test_forward_tiny_all_tokens()                          # the library still works
 
 
 def test_forward_identical_experts_reduce_to_one():

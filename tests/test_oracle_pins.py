@@ -702,6 +702,35 @@ def _ste(v, value):
     return v + (torch.as_tensor(value, dtype=torch.float64) - v).detach()
 
 
+def test_forward_gu_is_the_exact_sum_rounded_to_fp32():
+    """oracle.qat.forward_gu (the g, u the backward's SwiGLU uses) equals, for
+    every channel, the correctly rounded float32 of the exact dot product of the
+    dequantised FP8 token and FP4 weight row (math.fsum of exact products; a
+    float32 tie would show as one ulp), and the C oracle's h of the same pair
+    is silu(g) * u of those values."""
+    from oracle import qat
+    rng = np.random.default_rng(31)
+    E, inter, d = 3, 128, 256
+    w13 = (rng.normal(0, 1, (E, 2 * inter, d)) / math.sqrt(d)).astype(np.float32)
+    w2 = (rng.normal(0, 1, (E, d, inter)) / math.sqrt(inter)).astype(np.float32)
+    f13, s13 = oracle.pack_fp4(w13)
+    f2, s2 = oracle.pack_fp4(w2)
+    W13 = np_dequant_fp4(f13, s13)
+    xb = bf16_bits_of(rng.normal(0, 1, (2, d)))
+    xq, xs = oracle.quant_act(xb)
+    for t in range(2):
+        xd = t_e4m3_decode(xq[t]) * np.ldexp(1.0, np.repeat(xs[t].astype(np.int64) - 127, 128))
+        for e in range(E):
+            g, u = qat.forward_gu(xq[t], xs[t], e, f13, s13)
+            exact = np.array([math.fsum(xd * W13[e, n]) for n in range(2 * inter)])
+            want = exact.astype(np.float32).astype(np.float64)
+            got = np.concatenate([g, u])
+            ulp = np.spacing(np.abs(want).astype(np.float32)).astype(np.float64)
+            assert np.all(np.abs(got - want) <= ulp)
+            h, _, _, _ = oracle.expert_pair(xq[t], xs[t], e, f13, s13, f2, s2)
+            assert np.allclose(h, (g / (1.0 + np.exp(-g)) * u).astype(np.float32), rtol=1e-6, atol=0)
+
+
 @pytest.mark.parametrize("quantize_grads", [False, True])
 def test_qat_backward_matches_autograd(quantize_grads):
     """The oracle's backward step equals PyTorch float64 autograd of the same
