@@ -103,6 +103,12 @@ constexpr uint32_t SFB_COL0 = 256;
 constexpr uint32_t SFB_COLS_PER_STAGE = 8;
 constexpr uint32_t SFA_COL0 = SFB_COL0 + 6 * SFB_COLS_PER_STAGE;   // after the deepest ring's B columns
 static_assert(SFA_COL0 + 2 * 4 <= TMEM_COLS, "tensor memory budget");
+// The backward's epilogue (MODE 3) parks 96 of each thread's 128 accumulator
+// columns here (96 per epilogue warp of a lane quarter), so that it can
+// release the accumulator at once without holding all 128 in registers.
+constexpr uint32_t STASH_COLS = 96;
+constexpr uint32_t STASH_COL0 = SFA_COL0 + 2 * 4;
+static_assert(STASH_COL0 + 2 * STASH_COLS <= TMEM_COLS, "tensor memory budget");
 // Full-barrier arrivals: the producer's expect_tx arrival alone (every copy
 // into a stage is a TMA or bulk copy counted in transaction bytes).
 __host__ __device__ constexpr uint32_t full_arrivals(int) { return 1; }
@@ -124,6 +130,16 @@ __host__ __device__ constexpr uint32_t idesc_base()
            ((uint32_t)(BM >> 4) << 24);
 }
 
+// SwiGLU backward of one channel (the backward GEMM's epilogue):
+//   dg = dh u s (1 + g (1 - s)),  du = dh g s,  s = 1 / (1 + e^-g),
+// with the hardware exp2 and reciprocal approximations and every other
+// rounding explicit, so that the epilogue's two passes get the same bits.
+__device__ __forceinline__ void swiglu_backward(float dh, float g, float u, float &dg, float &du)
+{
+    const float s = __fdividef(1.0f, __fadd_rn(1.0f, __expf(-g)));
+    dg = __fmul_rn(__fmul_rn(__fmul_rn(dh, u), s), __fmaf_rn(g, __fsub_rn(1.0f, s), 1.0f));
+    du = __fmul_rn(__fmul_rn(dh, g), s);
+}
 
 struct Tile {
     int e, m_tile, n_block, row0, valid;   // m_tile: index of the row tile among all experts' tiles
@@ -490,6 +506,14 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
         for (long long tile = blockIdx.x; q < C::EPI_Q && tile < total_tiles && !*abort_flag;
              tile += gridDim.x) {
             const Tile ti = decode_tile(tile, s_tp, s_offs, E, nb, TR);
+            if (MODE == 3 && r < ti.valid) {
+                // the backward's epilogue reads this row's g and u of the tile's
+                // channels: start bringing them into L2 while the tile accumulates
+                const float *gp = g.gu_in + ((size_t)ti.row0 + r) * (2 * (size_t)out_dim) +
+                                  (size_t)ti.n_block * BN + 128 * half;
+                prefetch_l2_bulk(gp, 128 * sizeof(float));
+                prefetch_l2_bulk(gp + out_dim, 128 * sizeof(float));
+            }
             if (!mbar_wait(acc_full, acc_phase, tmo, abort_flag)) {
                 *abort_flag = 1;
                 break;
@@ -579,88 +603,99 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 // SwiGLU backward with the forward's g and u:
                 //   dg = dh u s (1 + g (1 - s)),  du = dh g s,  s = 1 / (1 + e^-g);
                 // [dg; du] quantised to E4M3 with one power-of-two scale per 128
-                // channels (the activations' rule).  Pass 0 finds the two amaxes,
-                // pass 1 recomputes and stores; the accumulator is released after.
+                // channels (the activations' rule).  The accumulator is released
+                // at once: the thread's columns 32..127 are parked in spare
+                // tensor-memory columns and 0..31 kept in registers, so the next
+                // tile's MMAs run while this tile's g and u (prefetched into L2
+                // while it accumulated) are read.  Pass 0 finds the two amaxes,
+                // pass 1 recomputes and stores.
                 const int I = out_dim;
                 const int c0 = ti.n_block * BN + 128 * half;
                 const bool live = r < ti.valid;
                 const float *grow = g.gu_in + row * (2 * (size_t)I);
-                float amax_g = 0.f, amax_u = 0.f, sg = 1.f, su = 1.f;
-                int eg = 0, eu = 0;
-                for (int pass = 0; pass < 2; pass++) {
-#pragma unroll 1
-                    for (int ch = 0; ch < 4; ch++) {
-                        uint32_t v[32], gv[32], uv[32];
-                        tmem_ld32(trow + 128 * half + 32 * ch, v);
-                        tmem_ld_wait();
+                const uint32_t stash = tmem + ((uint32_t)(q * 32) << 16) + STASH_COL0 + STASH_COLS * half;
+                uint32_t v0[32], w[32];
 #pragma unroll
-                        for (int q8 = 0; q8 < 4; q8++) {
-                            uint32_t a[8], b[8];
-                            if (live) {
-                                ld_global_nc_v8(a, grow + c0 + 32 * ch + 8 * q8);
-                                ld_global_nc_v8(b, grow + I + c0 + 32 * ch + 8 * q8);
-                            } else {
-#pragma unroll
-                                for (int u = 0; u < 8; u++) a[u] = b[u] = 0u;
-                            }
-#pragma unroll
-                            for (int u = 0; u < 8; u++) {
-                                gv[8 * q8 + u] = a[u];
-                                uv[8 * q8 + u] = b[u];
-                            }
-                        }
-                        float dg[32], du[32];
-#pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            const float dh = __uint_as_float(v[i]), gg_ = __uint_as_float(gv[i]),
-                                        uu = __uint_as_float(uv[i]);
-                            const float sgm = __fdividef(1.0f, 1.0f + __expf(-gg_));
-                            dg[i] = dh * uu * sgm * (1.0f + gg_ * (1.0f - sgm));
-                            du[i] = dh * gg_ * sgm;
-                        }
-                        if (pass == 0) {
-#pragma unroll
-                            for (int i = 0; i < 32; i++) {
-                                amax_g = fmaxf(amax_g, fabsf(dg[i]));
-                                amax_u = fmaxf(amax_u, fabsf(du[i]));
-                            }
-                        } else if (live) {
-                            uint32_t wg[8], wu[8];
-#pragma unroll
-                            for (int u = 0; u < 8; u++) {
-                                wg[u] = cvt_e4m3x2(dg[4 * u] * sg, dg[4 * u + 1] * sg) |
-                                        (cvt_e4m3x2(dg[4 * u + 2] * sg, dg[4 * u + 3] * sg) << 16);
-                                wu[u] = cvt_e4m3x2(du[4 * u] * su, du[4 * u + 1] * su) |
-                                        (cvt_e4m3x2(du[4 * u + 2] * su, du[4 * u + 3] * su) << 16);
-                            }
-                            uint8_t *qrow = g.dgu + row * (2 * (size_t)I);
-                            st_global_v8(qrow + c0 + 32 * ch, wg);
-                            st_global_v8(qrow + I + c0 + 32 * ch, wu);
-                            if (g.dgu_f32) {
-                                float *frow = g.dgu_f32 + row * (2 * (size_t)I);
-#pragma unroll
-                                for (int q8 = 0; q8 < 4; q8++) {
-                                    uint32_t a[8], b[8];
-#pragma unroll
-                                    for (int u = 0; u < 8; u++) {
-                                        a[u] = __float_as_uint(dg[8 * q8 + u]);
-                                        b[u] = __float_as_uint(du[8 * q8 + u]);
-                                    }
-                                    st_global_v8(frow + c0 + 32 * ch + 8 * q8, a);
-                                    st_global_v8(frow + I + c0 + 32 * ch + 8 * q8, b);
-                                }
-                            }
-                        }
-                    }
-                    if (pass == 0) {
-                        eg = e4m3_scale_exp(amax_g);
-                        eu = e4m3_scale_exp(amax_u);
-                        sg = exp2i(-eg);
-                        su = exp2i(-eu);
-                    }
+                for (int c = 1; c < 4; c++) {
+                    tmem_ld32(trow + 128 * half + 32 * c, w);
+                    tmem_ld_wait();
+                    tmem_st32(stash + 32 * (c - 1), w);
                 }
+                tmem_ld32(trow + 128 * half, v0);
+                tmem_ld_wait();
+                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(acc_empty);
+                // 8 channels per step: j < 4 from the registers, the rest from the
+                // parked columns (32 at a time).  Every lane runs both passes
+                // (the tensor-memory loads are warp-collective); lanes of rows
+                // past the tile's last pair read zeros and store nothing.
+                float amax_g = 0.f, amax_u = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    if (j >= 4 && (j & 3) == 0) {
+                        tmem_ld32(stash + 32 * ((j >> 2) - 1), w);
+                        tmem_ld_wait();
+                    }
+                    const uint32_t *v = j < 4 ? v0 : w;
+                    uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0}, b[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    if (live) {
+                        ld_global_nc_v8(a, grow + c0 + 8 * j);
+                        ld_global_nc_v8(b, grow + I + c0 + 8 * j);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; u++) {
+                        float dg, du;
+                        swiglu_backward(__uint_as_float(v[8 * (j & 3) + u]), __uint_as_float(a[u]),
+                                        __uint_as_float(b[u]), dg, du);
+                        amax_g = fmaxf(amax_g, fabsf(dg));
+                        amax_u = fmaxf(amax_u, fabsf(du));
+                    }
+                }
+                const int eg = e4m3_scale_exp(amax_g), eu = e4m3_scale_exp(amax_u);
+                const float sg = exp2i(-eg), su = exp2i(-eu);
+                // pass 1's loads may not be hoisted into pass 0 (the scheduler
+                // would keep both passes' operands live): their addresses take a
+                // zero the compiler cannot see through, the sign bit of the
+                // non-negative amax
+                const float *grow1 = grow + (__float_as_uint(fmaxf(amax_g, amax_u)) >> 31);
+                uint8_t *qrow = g.dgu + row * (2 * (size_t)I);
+                float *frow = g.dgu_f32 ? g.dgu_f32 + row * (2 * (size_t)I) : nullptr;
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    if (j >= 4 && (j & 3) == 0) {
+                        tmem_ld32(stash + 32 * ((j >> 2) - 1), w);
+                        tmem_ld_wait();
+                    }
+                    const uint32_t *v = j < 4 ? v0 : w;
+                    uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0}, b[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    if (live) {
+                        ld_global_nc_v8(a, grow1 + c0 + 8 * j);
+                        ld_global_nc_v8(b, grow1 + I + c0 + 8 * j);
+                    }
+                    uint32_t pg[2], pu[2];
+#pragma unroll
+                    for (int h4 = 0; h4 < 2; h4++) {
+                        float dg[4], du[4];
+#pragma unroll
+                        for (int u = 0; u < 4; u++)
+                            swiglu_backward(__uint_as_float(v[8 * (j & 3) + 4 * h4 + u]),
+                                            __uint_as_float(a[4 * h4 + u]), __uint_as_float(b[4 * h4 + u]), dg[u],
+                                            du[u]);
+                        pg[h4] = cvt_e4m3x2(dg[0] * sg, dg[1] * sg) | (cvt_e4m3x2(dg[2] * sg, dg[3] * sg) << 16);
+                        pu[h4] = cvt_e4m3x2(du[0] * su, du[1] * su) | (cvt_e4m3x2(du[2] * su, du[3] * su) << 16);
+                        if (live && frow) {
+                            *reinterpret_cast<float4 *>(frow + c0 + 8 * j + 4 * h4) =
+                                make_float4(dg[0], dg[1], dg[2], dg[3]);
+                            *reinterpret_cast<float4 *>(frow + I + c0 + 8 * j + 4 * h4) =
+                                make_float4(du[0], du[1], du[2], du[3]);
+                        }
+                    }
+                    if (live) {
+                        *reinterpret_cast<uint2 *>(qrow + c0 + 8 * j) = make_uint2(pg[0], pg[1]);
+                        *reinterpret_cast<uint2 *>(qrow + I + c0 + 8 * j) = make_uint2(pu[0], pu[1]);
+                    }
+                }
                 if (live) {
                     uint8_t *srow = g.dgu_scale + row * (2 * (size_t)I / 128);
                     srow[c0 / 128] = (uint8_t)(eg + 127);

@@ -81,17 +81,20 @@ def forward(x: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
 
 
 class GraphedForward:
-    """A serving step captured once as a CUDA graph and replayed per step: copy
-    the step's tokens in from pinned host memory, run the layer forward,
-    copy the output back to pinned host memory.
+    """A serving step whose forward is captured once as a CUDA graph and
+    replayed per step: copy the step's tokens in from pinned host memory,
+    replay the forward, copy the output back to pinned host memory.
 
     The captured work is exactly that of ``forward`` (the same kernels, with
     programmatic dependent launch between them kept as graph edges), on
     device buffers owned by this object.  Replaying costs the host one graph
     launch instead of the argument marshalling and the per-kernel launches of
     an eager call, which matters when every step waits for its result (a
-    decode loop).  Inputs are read from ``x_host`` at replay time: write the
-    next step's tokens into it, then call ``replay``; ``out_host`` holds the
+    decode loop).  The two copies are issued around the replay rather than
+    captured: with them inside the graph, a step of 16384 tokens of width
+    7168 (235 MB each way) took 12.3 ms against 7.65 ms for the same eager
+    copies.  Inputs are read from ``x_host`` at replay time: write the next
+    step's tokens into it, then call ``replay``; ``out_host`` holds the
     result once the stream reaches the end of the replay.
     """
 
@@ -114,20 +117,89 @@ class GraphedForward:
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
-            self._body()                      # eager once: kernel attributes set outside the capture
+            self.x.copy_(self.x_host, non_blocking=True)
+            self._forward()                   # eager once: kernel attributes set outside the capture
         torch.cuda.current_stream(dev).wait_stream(side)
         torch.cuda.synchronize(dev)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
-            self._body()
+            self._forward()
 
-    def _body(self):
+    def _forward(self):
         gate_w, pk, k, gate_bias = self._args
-        self.x.copy_(self.x_host, non_blocking=True)
         capi.moe_forward_ex(self.x, gate_w, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, self.out, k,
                             gate_bias=gate_bias, workspace=self.ws)
-        self.out_host.copy_(self.out, non_blocking=True)
 
     def replay(self):
         """Enqueue one step on the current stream."""
+        self.x.copy_(self.x_host, non_blocking=True)
         self.graph.replay()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+
+class PipelinedForward:
+    """Consecutive serving steps with their host copies overlapped with the
+    layer's kernels: step i's tokens are copied in on one copy stream while
+    step i-1's forward runs, and its output is copied out on a second copy
+    stream while step i+1's forward runs.  ``depth`` device slots of x and out
+    alternate; one workspace serves every step, because the forwards run one
+    after another on the compute stream.  Events order each slot's reuse: a
+    slot's next copy-in waits for the forward that read it, and its next
+    forward for the copy-out that read its output.
+
+    ``step(x_host, out_host)`` enqueues one step and returns the event that
+    completes once ``out_host`` holds the result; ``x_host`` may be rewritten
+    once the step's copy-in is done (``in_event``).  Both must be pinned.
+    """
+
+    def __init__(self, T: int, d: int, gate_w: torch.Tensor, pk: PackedExperts, k: int,
+                 gate_bias: Optional[torch.Tensor] = None, depth: int = 2, stream=None):
+        if depth < 1:
+            raise ValueError("depth must be at least 1")
+        dev = gate_w.device
+        E = gate_w.shape[1]
+        inter = pk.w13_fp4.shape[1] // 2
+        self.depth = depth
+        self.x = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.out = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.ws = workspace(T, d, inter, E, k, dev)
+        self.compute = stream if stream is not None else torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.in_done = [torch.cuda.Event() for _ in range(depth)]
+        self.fwd_done = [torch.cuda.Event() for _ in range(depth)]
+        self.out_done = [torch.cuda.Event() for _ in range(depth)]
+        self._used = [False] * depth
+        self._args = (gate_w, pk, k, gate_bias)
+        self.i = 0
+        self.in_event = None
+
+    def step(self, x_host: torch.Tensor, out_host: torch.Tensor) -> torch.cuda.Event:
+        if not (x_host.is_pinned() and out_host.is_pinned()):
+            raise ValueError("x_host and out_host must be pinned host memory")
+        gate_w, pk, k, gate_bias = self._args
+        s = self.i % self.depth
+        if self._used[s]:
+            self.h2d.wait_event(self.fwd_done[s])          # the forward that read x[s] is done
+        with torch.cuda.stream(self.h2d):
+            self.x[s].copy_(x_host, non_blocking=True)
+            self.in_done[s].record(self.h2d)
+        self.compute.wait_event(self.in_done[s])
+        if self._used[s]:
+            self.compute.wait_event(self.out_done[s])      # the copy-out that read out[s] is done
+        capi.moe_forward_ex(self.x[s], gate_w, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, self.out[s], k,
+                            stream=self.compute, gate_bias=gate_bias, workspace=self.ws)
+        self.fwd_done[s].record(self.compute)
+        self.d2h.wait_event(self.fwd_done[s])
+        with torch.cuda.stream(self.d2h):
+            out_host.copy_(self.out[s], non_blocking=True)
+            self.out_done[s].record(self.d2h)
+        self._used[s] = True
+        self.in_event = self.in_done[s]
+        self.i += 1
+        return self.out_done[s]
+
+    def join(self):
+        """Make the compute stream wait for every copy enqueued so far."""
+        self.compute.wait_stream(self.h2d)
+        self.compute.wait_stream(self.d2h)
