@@ -129,7 +129,8 @@ def moe_pack_fp4(w, w_fp4, w_scale, stream=None):
 
 def moe_fp4_to_fp8t(w_fp4, w_scale, w8t, s8t, stream=None):
     """w_fp4 uint8 [E, N, K/2], w_scale [E, N, K/32] (moe_pack_fp4 output) ->
-    w8t uint8 [E, K, N] E4M3 codes, s8t uint8 [E, K/128, N/128] block exponents + 127."""
+    w8t uint8 [E, K, N] bytes: E4M3 codes of W^T in the header's tiled block order,
+    s8t uint8 [E, K/128, N/128] block exponents + 127."""
     E, N, K2 = w_fp4.shape
     _check(_lib.moe_fp4_to_fp8t(_ptr(w_fp4), _ptr(w_scale), _ptr(w8t), _ptr(s8t), E, N, 2 * K2, _stream(stream)),
            "moe_fp4_to_fp8t")

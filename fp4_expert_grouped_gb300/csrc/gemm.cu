@@ -359,8 +359,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                             tma_load_2d(sa, &tmA, fb, ks * BK, ti.row0);
                         }
                     }
-                    if (MODE == 3)   // FP8 weight rows [E * N][K]: the tile's 256 rows at K block ks
-                        tma_load_2d(sb, &tmB, fb, ks * BK, ti.e * g.N + ti.n_block * BN);
+                    if (MODE == 3)   // tiled FP8 weights: the tile's two 128-row blocks at K block ks, 32 KB
+                        tma_load_2d(sb, &tmB, fb, 0, (int)(fp8t_block(ti.e, 2 * ti.n_block, ks, g.N, g.K) * 128));
                     else
                         tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk + bstride * ks));
                     if ((ks & 3) == 0)
@@ -626,31 +626,46 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(acc_empty);
-                // 8 channels per step: j < 4 from the registers, the rest from the
-                // parked columns (32 at a time).  Every lane runs both passes
-                // (the tensor-memory loads are warp-collective); lanes of rows
-                // past the tile's last pair read zeros and store nothing.
+                // 32 channels per group: the group's g and u (eight 32-byte loads
+                // per lane, issued together so that one memory round trip
+                // serves the group), then its dh (group 0 from the registers,
+                // the others from the parked columns).  The loads do not
+                // allocate in L1: each lane reads its own row, 32 rows per warp
+                // load, and caching those lines in L1 (the default for
+                // read-only loads) made the whole kernel 1.8x slower at 16K
+                // tokens (4.0 -> 2.26 ms), the operand pipeline starved.  Every
+                // lane runs both passes (the tensor-memory loads are
+                // warp-collective); lanes of rows past the tile's last pair
+                // read zeros and store nothing.
                 float amax_g = 0.f, amax_u = 0.f;
 #pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    if (j >= 4 && (j & 3) == 0) {
-                        tmem_ld32(stash + 32 * ((j >> 2) - 1), w);
+                for (int c = 0; c < 4; c++) {
+                    uint32_t a[4][8], b[4][8];
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; q8++) {
+                        if (live) {
+                            ld_global_nc_na_v8(a[q8], grow + c0 + 32 * c + 8 * q8);
+                            ld_global_nc_na_v8(b[q8], grow + I + c0 + 32 * c + 8 * q8);
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 8; u++) a[q8][u] = b[q8][u] = 0u;
+                        }
+                    }
+                    if (c > 0) {
+                        tmem_ld32(stash + 32 * (c - 1), w);
                         tmem_ld_wait();
                     }
-                    const uint32_t *v = j < 4 ? v0 : w;
-                    uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0}, b[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    if (live) {
-                        ld_global_nc_v8(a, grow + c0 + 8 * j);
-                        ld_global_nc_v8(b, grow + I + c0 + 8 * j);
-                    }
+                    const uint32_t *v = c == 0 ? v0 : w;
 #pragma unroll
-                    for (int u = 0; u < 8; u++) {
-                        float dg, du;
-                        swiglu_backward(__uint_as_float(v[8 * (j & 3) + u]), __uint_as_float(a[u]),
-                                        __uint_as_float(b[u]), dg, du);
-                        amax_g = fmaxf(amax_g, fabsf(dg));
-                        amax_u = fmaxf(amax_u, fabsf(du));
-                    }
+                    for (int q8 = 0; q8 < 4; q8++)
+#pragma unroll
+                        for (int u = 0; u < 8; u++) {
+                            float dg, du;
+                            swiglu_backward(__uint_as_float(v[8 * q8 + u]), __uint_as_float(a[q8][u]),
+                                            __uint_as_float(b[q8][u]), dg, du);
+                            amax_g = fmaxf(amax_g, fabsf(dg));
+                            amax_u = fmaxf(amax_u, fabsf(du));
+                        }
                 }
                 const int eg = e4m3_scale_exp(amax_g), eu = e4m3_scale_exp(amax_u);
                 const float sg = exp2i(-eg), su = exp2i(-eu);
@@ -662,38 +677,48 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 uint8_t *qrow = g.dgu + row * (2 * (size_t)I);
                 float *frow = g.dgu_f32 ? g.dgu_f32 + row * (2 * (size_t)I) : nullptr;
 #pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    if (j >= 4 && (j & 3) == 0) {
-                        tmem_ld32(stash + 32 * ((j >> 2) - 1), w);
-                        tmem_ld_wait();
-                    }
-                    const uint32_t *v = j < 4 ? v0 : w;
-                    uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0}, b[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    if (live) {
-                        ld_global_nc_v8(a, grow1 + c0 + 8 * j);
-                        ld_global_nc_v8(b, grow1 + I + c0 + 8 * j);
-                    }
-                    uint32_t pg[2], pu[2];
+                for (int c = 0; c < 4; c++) {
+                    uint32_t a[4][8], b[4][8];
 #pragma unroll
-                    for (int h4 = 0; h4 < 2; h4++) {
-                        float dg[4], du[4];
+                    for (int q8 = 0; q8 < 4; q8++) {
+                        if (live) {
+                            ld_global_nc_na_v8(a[q8], grow1 + c0 + 32 * c + 8 * q8);
+                            ld_global_nc_na_v8(b[q8], grow1 + I + c0 + 32 * c + 8 * q8);
+                        } else {
 #pragma unroll
-                        for (int u = 0; u < 4; u++)
-                            swiglu_backward(__uint_as_float(v[8 * (j & 3) + 4 * h4 + u]),
-                                            __uint_as_float(a[4 * h4 + u]), __uint_as_float(b[4 * h4 + u]), dg[u],
-                                            du[u]);
-                        pg[h4] = cvt_e4m3x2(dg[0] * sg, dg[1] * sg) | (cvt_e4m3x2(dg[2] * sg, dg[3] * sg) << 16);
-                        pu[h4] = cvt_e4m3x2(du[0] * su, du[1] * su) | (cvt_e4m3x2(du[2] * su, du[3] * su) << 16);
-                        if (live && frow) {
-                            *reinterpret_cast<float4 *>(frow + c0 + 8 * j + 4 * h4) =
-                                make_float4(dg[0], dg[1], dg[2], dg[3]);
-                            *reinterpret_cast<float4 *>(frow + I + c0 + 8 * j + 4 * h4) =
-                                make_float4(du[0], du[1], du[2], du[3]);
+                            for (int u = 0; u < 8; u++) a[q8][u] = b[q8][u] = 0u;
                         }
                     }
+                    if (c > 0) {
+                        tmem_ld32(stash + 32 * (c - 1), w);
+                        tmem_ld_wait();
+                    }
+                    const uint32_t *v = c == 0 ? v0 : w;
+                    uint32_t wg[8], wu[8];               // one 32-byte sector of codes per lane each
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; q8++)
+#pragma unroll
+                        for (int h4 = 0; h4 < 2; h4++) {
+                            float dg[4], du[4];
+#pragma unroll
+                            for (int u = 0; u < 4; u++)
+                                swiglu_backward(__uint_as_float(v[8 * q8 + 4 * h4 + u]),
+                                                __uint_as_float(a[q8][4 * h4 + u]),
+                                                __uint_as_float(b[q8][4 * h4 + u]), dg[u], du[u]);
+                            wg[2 * q8 + h4] =
+                                cvt_e4m3x2(dg[0] * sg, dg[1] * sg) | (cvt_e4m3x2(dg[2] * sg, dg[3] * sg) << 16);
+                            wu[2 * q8 + h4] =
+                                cvt_e4m3x2(du[0] * su, du[1] * su) | (cvt_e4m3x2(du[2] * su, du[3] * su) << 16);
+                            if (live && frow) {
+                                *reinterpret_cast<float4 *>(frow + c0 + 32 * c + 8 * q8 + 4 * h4) =
+                                    make_float4(dg[0], dg[1], dg[2], dg[3]);
+                                *reinterpret_cast<float4 *>(frow + I + c0 + 32 * c + 8 * q8 + 4 * h4) =
+                                    make_float4(du[0], du[1], du[2], du[3]);
+                            }
+                        }
                     if (live) {
-                        *reinterpret_cast<uint2 *>(qrow + c0 + 8 * j) = make_uint2(pg[0], pg[1]);
-                        *reinterpret_cast<uint2 *>(qrow + I + c0 + 8 * j) = make_uint2(pu[0], pu[1]);
+                        st_global_v8(qrow + c0 + 32 * c, wg);
+                        st_global_v8(qrow + I + c0 + 32 * c, wu);
                     }
                 }
                 if (live) {
@@ -853,12 +878,14 @@ static cudaError_t launch_gemm(const GemmArgs &a, int out_dim, cudaStream_t st)
 
 // FP8 weight rows [rows][K] (the backward's transposed weights), a 128-byte x
 // 256-row box, 128-byte swizzle
-static bool make_map_fp8_rows(CUtensorMap *m, const uint8_t *b, long long rows, int K)
+// The tiled FP8 weights of moe_fp4_to_fp8t as rows of 128 bytes (every block
+// row); a box is 256 of them: two neighbouring blocks, 128-byte swizzle.
+static bool make_map_fp8_tiled(CUtensorMap *m, const uint8_t *b, long long rows)
 {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint64_t dims[2] = {(cuuint64_t)gg::BK, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)gg::BK};
     cuuint32_t box[2] = {(cuuint32_t)gg::BK, (cuuint32_t)gg::BN};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(b), dims, strides, box, es,
@@ -871,7 +898,7 @@ cudaError_t launch_gemm_dgrad_h(const GemmArgs &a, int inter, cudaStream_t st)
     if (a.P == 0) return cudaSuccess;
     CUtensorMap ma, ma2, mb;
     if (!make_map_a(&ma, a.a, a.a_rows, a.K, gg::BM) || !make_map_a(&ma2, a.a, a.a_rows, a.K, gg::A_SMALL_ROWS) ||
-        !make_map_fp8_rows(&mb, a.b, (long long)a.E * a.N, a.K))
+        !make_map_fp8_tiled(&mb, a.b, (long long)a.E * a.N * (a.K / 128)))
         return cudaErrorInvalidValue;
     auto kern = gg::grouped_gemm_kernel<3, false, 128>;
     int smem = gg::Cfg<128>::SMEM_BYTES, threads = gg::Cfg<128>::NUM_THREADS;

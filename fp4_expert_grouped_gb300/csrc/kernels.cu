@@ -103,6 +103,7 @@ __device__ __forceinline__ float pow2_any(int e)
 }
 
 constexpr int kF8tRow = 64;                   // shared-memory row of 128 codes
+constexpr long long kF8tBlockBytes = 128 * 128;   // one 128 x 128 block of E4M3 codes
 
 __global__ void __launch_bounds__(256) fp4_to_fp8t_kernel(const uint8_t *__restrict__ w_fp4,
                                                           const uint8_t *__restrict__ w_scale,
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(256) fp4_to_fp8t_kernel(const uint8_t *__restr
             if (u & 1) out[u >> 1] |= c2 << 16;
             else out[u >> 1] = c2;
         }
-        uint8_t *dst = w8t + ((long long)e * K + (long long)bk * 128 + k) * N + (long long)bn * 128 + n0;
+        uint8_t *dst = w8t + fp8t_block(e, bk, bn, K, N) * kF8tBlockBytes + k * 128 + n0;
         *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
     }
     pdl_trigger();

@@ -142,6 +142,15 @@ __device__ __forceinline__ void ld_global_ro_v8(uint32_t (&w)[8], const void *p)
         : "l"(p));
 }
 
+// 32-byte read-only global load that does not allocate in L1 (data read once
+// per pass by one lane: caching it there only takes the L1 from the others).
+__device__ __forceinline__ void ld_global_nc_na_v8(uint32_t (&w)[8], const void *p)
+{
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
 // Bring [p, p + bytes) into L2 ahead of use (p 16-byte aligned, bytes a
 // multiple of 16); no completion to wait for.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)

@@ -52,6 +52,21 @@ __host__ __device__ inline long long weight_block(long long e, int n128, int k12
     const long long base = e * NB * KB;
     return j < NB / 2 ? base + ((long long)j * KB + k128) * 2 + h : base + 2LL * (NB / 2) * KB + k128;
 }
+
+// Block number of 128 x 128 block (rb, cb) of expert e's transposed FP8
+// weights (moe_fp4_to_fp8t: R = K rows, C = N columns per expert, 16 KB per
+// block, row r at r * 128).  Row blocks pair as (2j, 2j + 1): a pair's two
+// blocks are neighbours at every column block, so the backward GEMM's 256-row
+// operand of one K stage is 32 KB of contiguous memory; with R/128 odd the
+// last row block is alone, its column blocks consecutive after the pairs'.
+__host__ __device__ inline long long fp8t_block(int e, int rb, int cb, int R, int C)
+{
+    const int RB = R / 128, CB = C / 128, J = RB / 2;
+    const long long base = (long long)e * RB * CB;
+    const int j = rb >> 1;
+    return j < J ? base + ((long long)j * CB + cb) * 2 + (rb & 1) : base + 2LL * J * CB + cb;
+}
+
 __host__ __device__ inline int sf_byte(int r, int j) { return (r % 32) * 16 + (r / 32) * 4 + j; }
 
 // Activation scales of the GEMM operands (xq rows for GEMM1, hq rows for

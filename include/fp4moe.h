@@ -107,8 +107,15 @@ moe_status moe_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale,
  * nearest even -- exactly the FP4 value over 2^B when X - B >= -8, i.e. when
  * the block's sub-block scales span at most 2^14.
  *   w_fp4, w_scale  device, moe_pack_fp4 output (tiled layout) of W [E][N][K]
- *   w8t             device, E*K*N bytes: E4M3 code of W[e][n][k] at
- *                   (e * K + k) * N + n (transposed, N contiguous), 16-byte aligned
+ *   w8t             device, E*K*N bytes, 16-byte aligned: the transposed
+ *                   matrix W[e]^T ([K][N]) in 128 x 128 blocks of 16 KB, the
+ *                   E4M3 code of W[e][n][k] at byte (k % 128) * 128 + n % 128
+ *                   of block fp8t(e, k/128, n/128); row blocks pair as
+ *                   (2j, 2j+1) with RB = K/128, CB = N/128, J = RB/2:
+ *                     fp8t(e, rb, cb) = e*RB*CB + ((rb/2)*CB + cb)*2 + rb%2
+ *                   for rb < 2J, and e*RB*CB + 2*J*CB + cb for an odd last
+ *                   row block (so the backward GEMM reads 256 rows of one
+ *                   K stage as 32 KB of contiguous memory)
  *   s8t             device, E*(K/128)*(N/128) bytes: B + 127 of block (bn, bk)
  *                   at (e * K/128 + bk) * N/128 + bn
  * Requires N % 128 == 0, K % 128 == 0.  Argument errors are reported before

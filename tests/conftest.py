@@ -44,6 +44,29 @@ def weight_block(e, n128, k128, N, K):
     return base + (j * KB + k128) * 2 + h if j < NB // 2 else base + 2 * (NB // 2) * KB + k128
 
 
+def fp8t_block(e, rb, cb, R, C):
+    """Block number of 128 x 128 block (rb, cb) of expert e's transposed FP8
+    weights ([R][C] per expert): row blocks pair as (2j, 2j + 1), a pair's two
+    blocks neighbours at every column block; an odd last row block alone, its
+    column blocks after the pairs'."""
+    RB, CB = R // 128, C // 128
+    J = RB // 2
+    base = e * RB * CB
+    return base + ((rb // 2) * CB + cb) * 2 + rb % 2 if rb // 2 < J else base + 2 * J * CB + cb
+
+
+def tile_fp8t(w8t):
+    """plain transposed codes [E][R][C] -> tiled bytes [E * RB * CB blocks][128][128]."""
+    import numpy as np
+    E, R, C = w8t.shape
+    out = np.empty((E * (R // 128) * (C // 128), 128, 128), np.uint8)
+    for rb in range(R // 128):
+        for cb in range(C // 128):
+            idx = [fp8t_block(e, rb, cb, R, C) for e in range(E)]
+            out[idx] = w8t[:, rb * 128:(rb + 1) * 128, cb * 128:(cb + 1) * 128]
+    return out
+
+
 def tile_codes(fp4):
     """plain codes [E][N][K/2] -> tiled bytes [E * NB * KB blocks][128 rows][64]."""
     import numpy as np

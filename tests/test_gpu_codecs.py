@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import oracle
-from conftest import tile_codes, tile_scales
+from conftest import tile_codes, tile_fp8t, tile_scales
 
 pytestmark = pytest.mark.gpu
 
@@ -133,8 +133,9 @@ def test_fp4_to_fp8t_bitexact(E, N, K):
     of, os_ = oracle.pack_fp4(w)
     rw, rs = oracle.fp4_to_fp8t(of, os_)
     assert np.array_equal(s8t.cpu().numpy(), rs)
-    got = w8t.cpu().numpy()
-    if not np.array_equal(got, rw):
-        bad = np.argwhere(got != rw)[:4]
-        pytest.fail("codes differ at (e, k, n) %s" % bad.tolist())
+    got = w8t.cpu().numpy().reshape(-1, 128, 128)
+    want = tile_fp8t(rw)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)[:4]
+        pytest.fail("codes differ at (block, row, column) %s" % bad.tolist())
     assert c.moe_get_device_status() == 0
