@@ -59,7 +59,8 @@ def parse():
                          "the workload's W13 and W2 shapes and print one JSON line per matrix")
     ap.add_argument("--dgrad", action="store_true",
                     help="instead of the layer: time moe_backward_h (the backward's dh = W2^T dy GEMM with the "
-                         "SwiGLU backward, QAT) on the workload, against its FP8 tensor-core roofline")
+                         "SwiGLU backward, QAT) and moe_backward_x (dx = W13^T [dg; du] summed over a token's "
+                         "slots) on the workload, against their FP8 tensor-core roofline; one JSON line each")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (a smaller case of the workload, e.g. for an ncu capture)")
     ap.add_argument("--experts", type=int, default=None,
@@ -627,14 +628,43 @@ def run_dgrad(args, w):
     st = capi.moe_get_device_status()
     if st != 0:
         raise RuntimeError("device status: " + capi.moe_status_string(st))
-    t = statistics.median(ms)
-    flops = 2.0 * w.P * w.d * w.inter
-    tf = flops / (t / 1e3) / 1e12
-    print(json.dumps({"metric": "moe_backward_h throughput (dh = W2^T dy + SwiGLU backward, FP8)",
-                      "config": config_of(w), "ms": t, "flops": flops, "value": tf, "unit": "TFLOP/s",
-                      "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_tflops, "unit": "TFLOP/s",
-                                   "peak_note": "FP8 = %.1f x %s bf16 burst" % (FP8_OVER_BF16, peak_src),
-                                   "frac": tf / fp8_tflops}}), flush=True)
+
+    def report(metric, t, flops):
+        tf = flops / (t / 1e3) / 1e12
+        print(json.dumps({"metric": metric, "config": config_of(w), "ms": t, "flops": flops, "value": tf,
+                          "unit": "TFLOP/s",
+                          "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_tflops, "unit": "TFLOP/s",
+                                       "peak_note": "FP8 = %.1f x %s bf16 burst" % (FP8_OVER_BF16, peak_src),
+                                       "frac": tf / fp8_tflops}}), flush=True)
+
+    report("moe_backward_h throughput (dh = W2^T dy + SwiGLU backward, FP8)", statistics.median(ms),
+           2.0 * w.P * w.d * w.inter)
+
+    # the second dgrad GEMM: dx = sum over slots of W13^T [dg; du]
+    del w8, s8
+    w8x = torch.empty((w.E, w.d, 2 * w.inter), dtype=torch.uint8, device=dev)
+    s8x = torch.empty((w.E, w.d // 128, 2 * w.inter // 128), dtype=torch.uint8, device=dev)
+    capi.moe_fp4_to_fp8t(pk.w13_fp4, pk.w13_scale, w8x, s8x)
+    dx = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=dev)
+    xws = torch.empty(capi.moe_backward_x_workspace_size(w.T, w.d, w.inter, w.E, w.k), dtype=torch.uint8,
+                      device=dev)
+    for _ in range(args.warmup):
+        capi.moe_backward_x(dgu, dgs, w8x, s8x, ws, dx, w.k, workspace=xws)
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        capi.moe_backward_x(dgu, dgs, w8x, s8x, ws, dx, w.k, workspace=xws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    st = capi.moe_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status: " + capi.moe_status_string(st))
+    report("moe_backward_x throughput (dx = W13^T [dg; du] summed over slots, FP8)", statistics.median(ms),
+           4.0 * w.P * w.d * w.inter)
 
 
 def main():

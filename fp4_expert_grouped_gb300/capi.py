@@ -36,7 +36,8 @@ MOE_GATE_TC_MIN_TOKENS = 1024
 # every symbol the header declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_fp4_to_fp8t", "moe_quantize_act", "moe_route",
            "moe_route_noalloc", "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
-           "moe_workspace_layout", "moe_get_device_status", "moe_backward_h", "moe_backward_h_workspace_size"]
+           "moe_workspace_layout", "moe_get_device_status", "moe_backward_h", "moe_backward_h_workspace_size",
+           "moe_backward_x", "moe_backward_x_workspace_size"]
 
 
 class MoeForwardOpts(ctypes.Structure):
@@ -79,6 +80,10 @@ _lib.moe_backward_h_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.moe_backward_h_workspace_size.restype = _sz
 _lib.moe_backward_h.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
 _lib.moe_backward_h.restype = _i
+_lib.moe_backward_x_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+_lib.moe_backward_x_workspace_size.restype = _sz
+_lib.moe_backward_x.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _i, _i, _i, _i, _i, _vp]
+_lib.moe_backward_x.restype = _i
 
 
 class MoeError(RuntimeError):
@@ -221,6 +226,22 @@ def moe_backward_h(dout, w2_fp8t, w2_s8t, gu, fwd_workspace, dgu, dgu_scale, k, 
                                _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
                                _ptr(dgu), _ptr(dgu_scale), _ptr(dgu_f32), T, d, inter, E, k, _stream(stream)),
            "moe_backward_h")
+
+
+def moe_backward_x_workspace_size(T, d, inter, E, k):
+    return _lib.moe_backward_x_workspace_size(T, d, inter, E, k)
+
+
+def moe_backward_x(dgu, dgu_scale, w13_fp8t, w13_s8t, fwd_workspace, dx, k, workspace=None, stream=None):
+    """dgu uint8 [T*k, 2*inter] + dgu_scale [T*k, 2*inter/128] (moe_backward_h outputs), w13_fp8t uint8
+    [E, d, 2*inter] + w13_s8t [E, d/128, 2*inter/128] (moe_fp4_to_fp8t of W13), fwd_workspace: the
+    forward's workspace; output dx bf16 [T, d]."""
+    T, d = dx.shape
+    E, _, twoI = w13_fp8t.shape
+    _check(_lib.moe_backward_x(_ptr(dgu), _ptr(dgu_scale), _ptr(w13_fp8t), _ptr(w13_s8t), _ptr(fwd_workspace),
+                               _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+                               _ptr(dx), T, d, twoI // 2, E, k, _stream(stream)),
+           "moe_backward_x")
 
 
 def moe_get_device_status(stream=None):

@@ -20,13 +20,14 @@
 namespace fp4moe {
 
 // The weights' block exponents as the tensor cores' scale-factor image: for
-// expert e, 256-row block nb of W2^T ([inter][d]) and K block ks, two 512-byte
-// blocks (rows 0-127 and 128-255) at ((e * inter/256 + nb) * d/128 + ks) * 2 + h,
-// every byte of block h the exponent of 128 x 128 block (2 nb + h, ks) -- the
-// tiled scale layout of moe_pack_fp4 with N = inter, K = d, all four 1 x 32
-// scales of a row equal.  One thread per 16 bytes.
+// expert e, 256-row block nb of W^T ([R][C]: W2^T with R = inter, C = d, or
+// W13^T with R = d, C = 2 inter) and K block ks, two 512-byte blocks (rows
+// 0-127 and 128-255) at ((e * R/256 + nb) * C/128 + ks) * 2 + h, every byte of
+// block h the exponent of 128 x 128 block (2 nb + h, ks) -- the tiled scale
+// layout of moe_pack_fp4 with N = R, K = C, all four 1 x 32 scales of a row
+// equal.  One thread per 16 bytes.
 __global__ void __launch_bounds__(256) bwd_scale_image_kernel(const uint8_t *__restrict__ s8t, uint8_t *__restrict__ img,
-                                                              long long n16, int inter, int d)
+                                                              long long n16, int R, int C)
 {
     pdl_wait();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -34,13 +35,13 @@ __global__ void __launch_bounds__(256) bwd_scale_image_kernel(const uint8_t *__r
         const long long b = i / 32;                       // 512-byte block
         const int h = (int)(b & 1);
         const long long q = b >> 1;
-        const int KB = d / 128, J = inter / 256;
+        const int KB = C / 128, J = R / 256;
         const int ks = (int)(q % KB);
         const long long ej = q / KB;
         const int nb = (int)(ej % J);
         const long long e = ej / J;
-        // s8t of W2 ([E][d][inter]) as moe_fp4_to_fp8t writes it: [E][inter/128][d/128]
-        const uint32_t v = s8t[(e * (inter / 128) + 2 * nb + h) * KB + ks];
+        // s8t as moe_fp4_to_fp8t writes it: [E][R/128][C/128]
+        const uint32_t v = s8t[(e * (R / 128) + 2 * nb + h) * KB + ks];
         const uint32_t w = v * 0x01010101u;
         reinterpret_cast<uint4 *>(img)[i] = make_uint4(w, w, w, w);
     }
@@ -104,6 +105,31 @@ __global__ void __launch_bounds__(256) bwd_dy_kernel(const uint16_t *__restrict_
     pdl_trigger();
 }
 
+// [dg; du]'s scales, row-major [P][G] (G = 2 inter / 128) as moe_backward_h
+// writes them, into the GEMM's per-tile scale layout: row r of row tile m,
+// 128-channel group grp at (m * stage_groups(2 inter) + grp / 4) * 512 +
+// sf_byte(r, grp % 4).  One thread per byte.
+__global__ void __launch_bounds__(256) bwd_sf_tiles_kernel(const uint8_t *__restrict__ scale,
+                                                           const int32_t *__restrict__ topk_idx,
+                                                           const int32_t *__restrict__ sorted_pair,
+                                                           const int32_t *__restrict__ expert_offsets,
+                                                           const int32_t *__restrict__ tile_prefix,
+                                                           uint8_t *__restrict__ tiles, long long P, int G, int k, int R)
+{
+    pdl_wait();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < P * G) {
+        const long long pos = i / G;
+        const int grp = (int)(i % G);
+        const int e = topk_idx[sorted_pair[pos]];
+        const int local = (int)(pos - expert_offsets[e]);
+        const long long m = tile_prefix[e] + local / R;
+        const int r = local % R;
+        tiles[(m * stage_groups(G * 128) + grp / 4) * kBlockScaleBytes + sf_byte(r, grp % 4)] = scale[i];
+    }
+    pdl_trigger();
+}
+
 namespace {
 
 bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -132,6 +158,24 @@ BwdLayout bwd_layout(int T, int d, int inter, int E, int k)
     l.dys = round_up256((size_t)P * d);
     l.img = l.dys + round_up256(tiles * stage_groups(d) * kBlockScaleBytes);
     l.total = l.img + round_up256((size_t)E * (inter / 128) * (d / 128) * kBlockScaleBytes);
+    return l;
+}
+
+// scratch of moe_backward_x: each pair's dx (bf16 [P][d]), the [dg; du] scales
+// in tile layout, the scale image of W13^T
+struct BwdXLayout {
+    size_t dxp, sft, img, total;
+};
+BwdXLayout bwdx_layout(int T, int d, int inter, int E, int k)
+{
+    const long long P = (long long)T * k;
+    const int R = gemm_tile_rows(P, E);
+    const size_t tiles = (size_t)max_row_tiles(P, E, R);
+    BwdXLayout l;
+    l.dxp = 0;
+    l.sft = round_up256((size_t)P * d * 2);
+    l.img = l.sft + round_up256(tiles * stage_groups(2 * inter) * kBlockScaleBytes);
+    l.total = l.img + round_up256((size_t)E * (d / 128) * (2 * inter / 128) * kBlockScaleBytes);
     return l;
 }
 
@@ -221,6 +265,92 @@ extern "C" moe_status moe_backward_h(const uint16_t *dout, const uint8_t *w2_fp8
         g.dgu_f32 = dgu_f32;
         e = launch_gemm_dgrad_h(g, inter, s);
     }
+    if (owned) {
+        cudaError_t f = cudaFreeAsync(base, s);
+        if (e == cudaSuccess) e = f;
+    }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" size_t moe_backward_x_workspace_size(int T, int d, int inter, int E, int k)
+{
+    if (!bwd_shape_ok(T, d, inter, E, k)) return 0;
+    return bwdx_layout(T, d, inter, E, k).total;
+}
+
+extern "C" moe_status moe_backward_x(const uint8_t *dgu, const uint8_t *dgu_scale, const uint8_t *w13_fp8t,
+                                     const uint8_t *w13_s8t, const void *fwd_workspace, void *workspace,
+                                     size_t workspace_bytes, uint16_t *dx, int T, int d, int inter, int E, int k,
+                                     void *stream)
+{
+    if (!dgu || !dgu_scale || !w13_fp8t || !w13_s8t || !fwd_workspace || !dx) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || d <= 0 || inter <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned_to(dgu, 16) || !aligned_to(w13_fp8t, 16) || !aligned_to(dx, 16) || !aligned_to(fwd_workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (!bwd_shape_ok(T, d, inter, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const BwdXLayout L = bwdx_layout(T, d, inter, E, k);
+    if (workspace && (!aligned_to(workspace, 256) || workspace_bytes < L.total)) return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    int num_sms = 0;
+    unsigned *status = nullptr;
+    moe_status st = device_query(&num_sms, &status);
+    if (st != MOE_OK) return st;
+    Workspace fw;
+    if (!workspace_layout(Shapes{T, d, inter, E, k}, &fw)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const uint8_t *fb = static_cast<const uint8_t *>(fwd_workspace);
+    const long long P = (long long)T * k;
+    const int R = gemm_tile_rows(P, E);
+    const int G = 2 * inter / 128;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(workspace);
+    bool owned = false;
+    if (!base) {
+        void *p = nullptr;
+        if (cudaMallocAsync(&p, L.total, s) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_WORKSPACE;
+        }
+        base = static_cast<uint8_t *>(p);
+        owned = true;
+    }
+    const int32_t *topk_idx = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_TOPK_IDX]);
+    const int32_t *offs = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_EXPERT_OFFSETS]);
+    const int32_t *sorted_pair = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_SORTED_PAIR]);
+    const int32_t *pair_pos = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_PAIR_POS]);
+    const int32_t *tile_prefix = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_TILE_PREFIX]);
+    uint16_t *dxp = reinterpret_cast<uint16_t *>(base + L.dxp);
+    uint8_t *sft = base + L.sft, *img = base + L.img;
+
+    const long long n16 = (long long)E * (d / 128) * G * (kBlockScaleBytes / 16);
+    cudaError_t e = launch_pdl(bwd_scale_image_kernel, dim3((unsigned)((n16 + 255) / 256)), dim3(256), 0, s, w13_s8t,
+                               img, n16, d, 2 * inter);
+    if (e == cudaSuccess)
+        e = launch_pdl(bwd_sf_tiles_kernel, dim3((unsigned)((P * G + 255) / 256)), dim3(256), 0, s, dgu_scale, topk_idx,
+                       sorted_pair, offs, tile_prefix, sft, P, G, k, R);
+    if (e == cudaSuccess) {
+        GemmArgs g;
+        std::memset(&g, 0, sizeof g);
+        g.tile_rows = R;
+        g.a = dgu;
+        g.a_scale_tiles = sft;
+        g.k = k;
+        g.a_rows = P;
+        g.b = w13_fp8t;
+        g.b_scale = img;
+        g.N = d;
+        g.K = 2 * inter;
+        g.expert_offsets = offs;
+        g.tile_prefix = tile_prefix;
+        g.E = E;
+        g.P = P;
+        g.y = dxp;
+        g.status = status;
+        g.timeout_ns = 2000000000ull;
+        g.num_sms = num_sms;
+        e = launch_gemm_dgrad_x(g, d, s);
+    }
+    if (e == cudaSuccess) e = launch_combine(dxp, pair_pos, nullptr, dx, T, d, k, s);
     if (owned) {
         cudaError_t f = cudaFreeAsync(base, s);
         if (e == cudaSuccess) e = f;

@@ -118,7 +118,7 @@ __host__ __device__ constexpr uint32_t full_arrivals(int) { return 1; }
 // count advances by the packed bytes: half the shared-memory footprint.
 // MODE 3 reads FP8 weights: one byte per code in global and shared memory.
 template <int MODE>
-__host__ __device__ constexpr uint32_t b_stage_tx() { return MODE == 3 ? B_STAGE : B_STAGE / 2; }
+__host__ __device__ constexpr uint32_t b_stage_tx() { return MODE >= 3 ? B_STAGE : B_STAGE / 2; }
 
 // Instruction descriptor of the block-scaled MMA: A = E4M3 (format 0), B =
 // E2M1 (format 5; E4M3 for the backward's FP8 weights, MODE 3), both K-major,
@@ -126,7 +126,7 @@ __host__ __device__ constexpr uint32_t b_stage_tx() { return MODE == 3 ? B_STAGE
 template <int MODE>
 __host__ __device__ constexpr uint32_t idesc_base()
 {
-    return (0u << 7) | ((MODE == 3 ? 0u : 5u) << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+    return (0u << 7) | ((MODE >= 3 ? 0u : 5u) << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
            ((uint32_t)(BM >> 4) << 24);
 }
 
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                             tma_load_2d(sa, &tmA, fb, ks * BK, ti.row0);
                         }
                     }
-                    if (MODE == 3)   // tiled FP8 weights: the tile's two 128-row blocks at K block ks, 32 KB
+                    if (MODE >= 3)   // tiled FP8 weights: the tile's two 128-row blocks at K block ks, 32 KB
                         tma_load_2d(sb, &tmB, fb, 0, (int)(fp8t_block(ti.e, 2 * ti.n_block, ks, g.N, g.K) * 128));
                     else
                         tma_load_3d(sb, &tmB, fb, 0, 0, (int)(blk + bstride * ks));
@@ -726,6 +726,33 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                     srow[c0 / 128] = (uint8_t)(eg + 127);
                     srow[(I + c0) / 128] = (uint8_t)(eu + 127);
                 }
+            } else if (MODE == 4) {
+                // Backward (QAT), dx of each pair: the accumulator holds output
+                // columns 256 n_block + 128 h .. +128 (the tile's two row blocks
+                // of W13^T are consecutive); rounded to bf16 like the forward's y
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(trow + 128 * half, v0);
+                tmem_ld32(trow + 128 * half + 32, v1);
+                tmem_ld32(trow + 128 * half + 64, v2);
+                tmem_ld32(trow + 128 * half + 96, v3);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+                if (r < ti.valid) {
+                    uint16_t *dst = g.y + row * out_dim + (size_t)ti.n_block * BN + 128 * half;
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const uint32_t *v = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int u = 0; u < 8; u++)
+                                w[u] = pack_bf16x2(__uint_as_float(v[16 * j + 2 * u]), __uint_as_float(v[16 * j + 2 * u + 1]));
+                            st_global_v8(dst + 32 * c + 16 * j, w);
+                        }
+                    }
+                }
             } else {
                 uint32_t v0[32], v1[32], v2[32], v3[32];
                 tmem_ld32(trow + 128 * half, v0);
@@ -893,25 +920,29 @@ static bool make_map_fp8_tiled(CUtensorMap *m, const uint8_t *b, long long rows)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_gemm_dgrad_h(const GemmArgs &a, int inter, cudaStream_t st)
+// The backward's GEMMs on the tiled FP8 weights: MODE 3 (dh = W2^T dy with the
+// SwiGLU backward, out_dim = inter) and MODE 4 (dx of each pair = W13^T [dg; du],
+// out_dim = d).
+template <int MODE>
+static cudaError_t launch_gemm_fp8b(const GemmArgs &a, int out_dim, cudaStream_t st)
 {
     if (a.P == 0) return cudaSuccess;
     CUtensorMap ma, ma2, mb;
     if (!make_map_a(&ma, a.a, a.a_rows, a.K, gg::BM) || !make_map_a(&ma2, a.a, a.a_rows, a.K, gg::A_SMALL_ROWS) ||
         !make_map_fp8_tiled(&mb, a.b, (long long)a.E * a.N * (a.K / 128)))
         return cudaErrorInvalidValue;
-    auto kern = gg::grouped_gemm_kernel<3, false, 128>;
+    auto kern = gg::grouped_gemm_kernel<MODE, false, 128>;
     int smem = gg::Cfg<128>::SMEM_BYTES, threads = gg::Cfg<128>::NUM_THREADS;
     if (a.tile_rows == 16) {
-        kern = gg::grouped_gemm_kernel<3, false, 16>;
+        kern = gg::grouped_gemm_kernel<MODE, false, 16>;
         smem = gg::Cfg<16>::SMEM_BYTES;
         threads = gg::Cfg<16>::NUM_THREADS;
     } else if (a.tile_rows == 32) {
-        kern = gg::grouped_gemm_kernel<3, false, 32>;
+        kern = gg::grouped_gemm_kernel<MODE, false, 32>;
         smem = gg::Cfg<32>::SMEM_BYTES;
         threads = gg::Cfg<32>::NUM_THREADS;
     } else if (a.tile_rows == 64) {
-        kern = gg::grouped_gemm_kernel<3, false, 64>;
+        kern = gg::grouped_gemm_kernel<MODE, false, 64>;
         smem = gg::Cfg<64>::SMEM_BYTES;
         threads = gg::Cfg<64>::NUM_THREADS;
     } else if (a.tile_rows != 128) {
@@ -919,10 +950,13 @@ cudaError_t launch_gemm_dgrad_h(const GemmArgs &a, int inter, cudaStream_t st)
     }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * (inter / gg::BN);
+    const long long tiles = max_row_tiles(a.P, a.E, a.tile_rows) * (out_dim / gg::BN);
     const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
-    return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ma, ma2, ma2, mb, a, inter);
+    return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ma, ma2, ma2, mb, a, out_dim);
 }
+
+cudaError_t launch_gemm_dgrad_h(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm_fp8b<3>(a, inter, st); }
+cudaError_t launch_gemm_dgrad_x(const GemmArgs &a, int d, cudaStream_t st) { return launch_gemm_fp8b<4>(a, d, st); }
 
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st) { return launch_gemm<1>(a, inter, st); }
 cudaError_t launch_gemm2(const GemmArgs &a, int d, cudaStream_t st) { return launch_gemm<2>(a, d, st); }

@@ -1089,6 +1089,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     pdl_wait();
     // one thread per 16 channels of a token: the k slot rows are loaded up
     // front (32 bytes each), then added in slot order with fused multiply-adds
+    // (weights 1 when topk_w is NULL: the backward's sum of a token's dx rows,
+    // a fused multiply-add by 1 being the plain fp32 sum)
     const int per_tok = d / 16;
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid >= (long long)T * per_tok) return;
@@ -1098,7 +1100,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
 #pragma unroll
     for (int j = 0; j < 8; j++) {
         if (j < k) {
-            w[j] = __ldg(topk_w + (size_t)t * k + j);
+            w[j] = topk_w ? __ldg(topk_w + (size_t)t * k + j) : 1.0f;
             const int pos = __ldg(pair_pos + (size_t)t * k + j);
             ld_global_nc_v8(v[j], y + (size_t)pos * d + 16 * c16);
         }

@@ -255,8 +255,12 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm1(const GemmArgs &a, int inter, cudaStream_t st);
 cudaError_t launch_gemm2(const GemmArgs &a, int d, cudaStream_t st);
-// dh = W2^T dy per pair on the FP8 weights (B = [E * inter][d] rows, scales in
-// the tiled scale layout with N = inter, K = d) with the SwiGLU backward fused
+// dh = W2^T dy per pair on the FP8 weights (B = W2^T in moe_fp4_to_fp8t's
+// 16 KB blocks, N = inter rows, K = d; scales as the block-exponent image in
+// the tiled scale layout) with the SwiGLU backward fused
 cudaError_t launch_gemm_dgrad_h(const GemmArgs &a, int inter, cudaStream_t st);
+// dx of every pair = W13^T [dg; du] on the FP8 W13 (B = W13^T in 16 KB blocks,
+// N = d rows, K = 2 inter), bf16 into y [P][d]
+cudaError_t launch_gemm_dgrad_x(const GemmArgs &a, int d, cudaStream_t st);
 
 } // namespace fp4moe

@@ -285,7 +285,8 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w,
  *   [dg; du] -> E4M3 codes with one power-of-two scale per 128 channels
  *   dout           device, bf16 [T][d]: the gradient at the layer output
  *   w2_fp8t        device, moe_fp4_to_fp8t output for W2 ([E][d][inter]): E4M3
- *                  [E][inter][d], 16-byte aligned
+ *                  codes of W2^T ([E][inter][d]) in that function's 16 KB
+ *                  blocks, 16-byte aligned
  *   w2_s8t         device, its block exponents [E][inter/128][d/128]
  *   gu             device, fp32 [T*k][2*inter] (moe_forward_opts.gu_out)
  *   fwd_workspace  device, the workspace of the forward call that produced gu
@@ -303,6 +304,34 @@ size_t moe_backward_h_workspace_size(int T, int d, int inter, int E, int k);
 moe_status moe_backward_h(const uint16_t *dout, const uint8_t *w2_fp8t, const uint8_t *w2_s8t, const float *gu,
                           const void *fwd_workspace, void *workspace, size_t workspace_bytes, uint8_t *dgu,
                           uint8_t *dgu_scale, float *dgu_f32, int T, int d, int inter, int E, int k, void *stream);
+
+/*
+ * moe_backward_x -- the second GEMM of the layer's backward pass (the same
+ * passages as moe_backward_h): the gradient at the layer input through the
+ * experts.  For every pair p = t*k + j routed to expert e, at its expert-order
+ * position pos:
+ *   dx_p   = W13[e]^T [dg; du]_p                          block-scaled FP8 MMA, fp32,
+ *                                                         rounded to bf16 (like y)
+ *   dx[t]  = bf16( sum over j = 0..k-1, in slot order, of dx_{t*k+j} )   fp32 sum
+ * (the routing weights' own gradient is not part of dx: routing is held fixed).
+ *   dgu, dgu_scale  device, moe_backward_h's outputs (E4M3 [T*k][2*inter] in
+ *                   expert order, 16-byte aligned, and [T*k][2*inter/128])
+ *   w13_fp8t        device, moe_fp4_to_fp8t output for W13 ([E][2*inter][d]):
+ *                   E4M3 codes of W13^T ([E][d][2*inter]) in 16 KB blocks,
+ *                   16-byte aligned
+ *   w13_s8t         device, its block exponents [E][d/128][2*inter/128]
+ *   fwd_workspace   device, the workspace of the forward call (routing and
+ *                   dispatch plan)
+ *   workspace       device scratch of moe_backward_x_workspace_size bytes,
+ *                   256-byte aligned, or NULL (then allocated stream-ordered)
+ *   dx              device, bf16 [T][d], 16-byte aligned
+ * Requires d % 256 == 0 and inter % 256 == 0, 1 <= k <= 8, k <= E <= 256.
+ * Argument errors are reported before anything is enqueued.
+ */
+size_t moe_backward_x_workspace_size(int T, int d, int inter, int E, int k);
+moe_status moe_backward_x(const uint8_t *dgu, const uint8_t *dgu_scale, const uint8_t *w13_fp8t,
+                          const uint8_t *w13_s8t, const void *fwd_workspace, void *workspace, size_t workspace_bytes,
+                          uint16_t *dx, int T, int d, int inter, int E, int k, void *stream);
 
 /* Bytes of workspace moe_forward_ex needs for these shapes (0 for bad shapes). */
 size_t moe_workspace_size(int T, int d, int inter, int E, int k);

@@ -148,3 +148,17 @@ def test_backward_h_argument_checks(capi):
     assert lib.moe_backward_h(F, F, F, F, F, None, 0, F, F, None, 0, 256, 256, 8, 2, None) == 0    # T == 0: no-op
     assert capi.moe_backward_h_workspace_size(8, 256, 384, 8, 2) == 0
     assert capi.moe_backward_h_workspace_size(8, 256, 256, 8, 2) > 0
+
+
+def test_backward_x_argument_checks(capi):
+    """moe_backward_x rejects bad shapes and pointers before touching CUDA."""
+    lib = capi.lib()
+    F = 0x100000
+    assert lib.moe_backward_x(F, F, F, F, F, None, 0, F, 8, 256, 384, 8, 2, None) == 2      # inter % 256
+    assert lib.moe_backward_x(F, F, F, F, F, None, 0, F, 8, 384, 256, 8, 2, None) == 2      # d % 256
+    assert lib.moe_backward_x(F, F, F, F, F, None, 0, None, 8, 256, 256, 8, 2, None) == 1   # no output
+    assert lib.moe_backward_x(F + 8, F, F, F, F, None, 0, F, 8, 256, 256, 8, 2, None) == 1  # dgu alignment
+    assert lib.moe_backward_x(F, F, F, F, F, F, 16, F, 8, 256, 256, 8, 2, None) == 4        # workspace too small
+    assert lib.moe_backward_x(F, F, F, F, F, None, 0, F, 0, 256, 256, 8, 2, None) == 0      # T == 0: no-op
+    assert capi.moe_backward_x_workspace_size(8, 256, 384, 8, 2) == 0
+    assert capi.moe_backward_x_workspace_size(8, 256, 256, 8, 2) > 0

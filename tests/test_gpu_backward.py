@@ -1,4 +1,5 @@
-"""The first GEMM of the QAT backward pass (moe_backward_h) against the oracle.
+"""The QAT backward pass's two dgrad GEMMs (moe_backward_h, moe_backward_x)
+against the oracle.
 
 dh = W2^T dy on the FP8 weights (moe_fp4_to_fp8t), the SwiGLU backward with
 the forward's g and u, [dg; du] quantised to E4M3 per 128 channels -- per
@@ -9,7 +10,10 @@ bf16), which makes the FP8 operand dy the same codes on both sides.  The
 unquantised dg, du must match at the layer tolerance (max|err| <= 1e-2
 max|ref|, per-pair relative L2 <= 5e-3); the E4M3 codes of [dg; du] are
 compared by fraction (a code flips where the GPU's fp32 sums and the oracle's
-float64 fall on two sides of a rounding boundary).
+float64 fall on two sides of a rounding boundary).  dx = sum over a token's
+slots of W13^T [dg; du] (oracle/qat.py: qat_backward) must match at the layer
+tolerance; the routing and plan the oracle side uses are its own, checked equal
+to the GPU's first.
 """
 import numpy as np
 import pytest
@@ -70,8 +74,29 @@ def run_backward(T, d, inter, E, k, seed, bias=False):
     again_s = torch.empty_like(dgs)
     c.moe_backward_h(dout.to(DEV), w8, s8, gu, ws, again, again_s, k)
     assert torch.equal(again, dgu) and torch.equal(again_s, dgs)          # deterministic
+    # dx through W13^T
+    w8x = torch.empty((E, d, 2 * inter), dtype=torch.uint8, device=DEV)
+    s8x = torch.empty((E, d // 128, 2 * inter // 128), dtype=torch.uint8, device=DEV)
+    c.moe_fp4_to_fp8t(pk.w13_fp4, pk.w13_scale, w8x, s8x)
+    dx = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    c.moe_backward_x(dgu, dgs, w8x, s8x, ws, dx, k)
+    dx2 = torch.empty_like(dx)
+    c.moe_backward_x(dgu, dgs, w8x, s8x, ws, dx2, k)
+    assert torch.equal(dx, dx2)                                          # deterministic
+    assert c.moe_get_device_status() == 0
     return dict(x=x, gw=gw, b=b, w13=w13, w2=w2, ti=ti.cpu().numpy(), pp=pp.cpu().numpy(), wts=wts.numpy(),
-                dout=dout, dgu=dgu.cpu().numpy(), dgs=dgs.cpu().numpy(), dgf=dgf.cpu().numpy().astype(np.float64))
+                dout=dout, dgu=dgu.cpu().numpy(), dgs=dgs.cpu().numpy(), dgf=dgf.cpu().numpy().astype(np.float64),
+                dx=inputs.bf16_bits(dx.cpu()))
+
+
+def oracle_routing(r, E, k):
+    """The oracle's own routing and dispatch plan of the case, checked equal to the GPU's."""
+    xb = inputs.bf16_bits(r["x"])
+    bias = None if r["b"] is None else r["b"].numpy()
+    ti, _ = oracle.route(xb, r["gw"].numpy(), k, bias)
+    _, _, pp = oracle.dispatch_plan(ti, E)
+    assert np.array_equal(ti, r["ti"]) and np.array_equal(pp, r["pp"])
+    return ti, pp
 
 
 def check_against_oracle(r, T, d, inter, E, k, pairs=None):
@@ -82,12 +107,13 @@ def check_against_oracle(r, T, d, inter, E, k, pairs=None):
     W2 = qat.fp8_weights(f2, s2)
     do = (inputs.bf16_bits(r["dout"]).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     E4M3 = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    ti, pp = oracle_routing(r, E, k)
     pairs = range(T * k) if pairs is None else pairs
     same_codes = same_scales = n_codes = n_scales = 0
     for p in pairs:
         t, j = divmod(p, k)
-        e = int(r["ti"][t, j])
-        pos = int(r["pp"][p])
+        e = int(ti[t, j])
+        pos = int(pp[p])
         g, u = qat.forward_gu(xq[t], xs[t], e, f13, s13)
         dy = float(r["wts"][j]) * do[t]
         dyq, dg, du, dgu = qat.pair_dgu(g, u, dy, W2[e], quantize_grads=True)
@@ -111,6 +137,22 @@ def check_against_oracle(r, T, d, inter, E, k, pairs=None):
     assert same_scales >= n_scales - max(1, n_scales // 200), (same_scales, n_scales)
 
 
+def check_dx_against_oracle(r, T, d, inter, E, k):
+    """dx of every token against the oracle's backward step (its own routing, the
+    test's routing weights, quantised gradients) at the layer tolerance."""
+    xb = inputs.bf16_bits(r["x"])
+    f13, s13 = oracle.pack_fp4(r["w13"].numpy())
+    f2, s2 = oracle.pack_fp4(r["w2"].numpy())
+    ti, _ = oracle_routing(r, E, k)
+    tw = np.tile(r["wts"], (T, 1)).astype(np.float32)
+    ref, _, _, _ = qat.qat_backward(xb, ti, tw, f13, s13, f2, s2, inputs.bf16_bits(r["dout"]), quantize_grads=True)
+    got = (r["dx"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    err = np.abs(got - ref)
+    assert err.max() <= 1e-2 * np.abs(ref).max(), (err.max(), np.abs(ref).max())
+    rel = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert rel.max() <= 5e-3, (rel.max(), int(rel.argmax()))
+
+
 @pytest.mark.parametrize("T,d,inter,E,k,bias", [
     (30, 256, 256, 8, 2, False),           # 16-row tiles (P <= 8 E)
     (60, 512, 256, 8, 2, True),            # 32-row tiles
@@ -118,6 +160,7 @@ def check_against_oracle(r, T, d, inter, E, k, pairs=None):
     (700, 256, 512, 8, 2, True),           # 128-row tiles, two 256-channel blocks of dh
     (64, 256, 256, 4, 4, False),           # k == E
 ])
-def test_backward_h_matches_oracle(T, d, inter, E, k, bias):
+def test_backward_matches_oracle(T, d, inter, E, k, bias):
     r = run_backward(T, d, inter, E, k, seed=T + d, bias=bias)
     check_against_oracle(r, T, d, inter, E, k)
+    check_dx_against_oracle(r, T, d, inter, E, k)
