@@ -666,6 +666,41 @@ def run_dgrad(args, w):
     report("moe_backward_x throughput (dx = W13^T [dg; du] summed over slots, FP8)", statistics.median(ms),
            4.0 * w.P * w.d * w.inter)
 
+    # the master weights' gradients: dW2 = sum dy (x) h, dW13 = sum [dg; du] (x) x per expert (bf16 tensor
+    # cores on the dequantised operands, fp32 out); bound by writing the fp32 gradients
+    del w8x, s8x, xws
+    dW13 = torch.empty((w.E, 2 * w.inter, w.d), dtype=torch.float32, device=dev)
+    dW2 = torch.empty((w.E, w.d, w.inter), dtype=torch.float32, device=dev)
+    wws = torch.empty(capi.moe_backward_w_workspace_size(w.T, w.d, w.inter, w.E, w.k), dtype=torch.uint8,
+                      device=dev)
+    for _ in range(args.warmup):
+        capi.moe_backward_w(ws, bws, dgu, dgs, dW13, dW2, w.k, workspace=wws)
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        capi.moe_backward_w(ws, bws, dgu, dgs, dW13, dW2, w.k, workspace=wws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    st = capi.moe_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status: " + capi.moe_status_string(st))
+    t = statistics.median(ms)
+    flops = 6.0 * w.P * w.d * w.inter
+    # algorithmic bytes: the fp32 gradients written, the E4M3 operands read once (dy, h, [dg; du] per pair,
+    # x per token with its scales)
+    by = 4.0 * w.E * 3 * w.d * w.inter + w.P * (w.d + w.inter + 2 * w.inter) + w.T * w.d
+    print(json.dumps({"metric": "moe_backward_w throughput (dW2, dW13 over each expert's pairs)",
+                      "config": config_of(w), "ms": t, "flops": flops, "bytes": by,
+                      "value": by / (t / 1e3) / 1e9, "unit": "GB/s",
+                      "roofline": {"bound": "hbm", "achieved": by / (t / 1e3) / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                                   "peak_note": "%s copy bandwidth" % peak_src,
+                                   "frac": by / (t / 1e3) / 1e9 / hbm_gbs},
+                      "tflops_bf16": flops / (t / 1e3) / 1e12}), flush=True)
+
 
 def main():
     args = parse()

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libfp4moe.so")
-SOURCES = ["api.cu", "kernels.cu", "gemm.cu", "gate_tc.cu", "backward.cu", "route_noalloc.cu"]
+SOURCES = ["api.cu", "kernels.cu", "gemm.cu", "gate_tc.cu", "backward.cu", "wgrad.cu", "route_noalloc.cu"]
 HEADERS = ["moe_device.cuh", "moe_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

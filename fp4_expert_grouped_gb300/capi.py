@@ -37,7 +37,8 @@ MOE_GATE_TC_MIN_TOKENS = 1024
 EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_fp4_to_fp8t", "moe_quantize_act", "moe_route",
            "moe_route_noalloc", "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
            "moe_workspace_layout", "moe_get_device_status", "moe_backward_h", "moe_backward_h_workspace_size",
-           "moe_backward_x", "moe_backward_x_workspace_size"]
+           "moe_backward_x", "moe_backward_x_workspace_size", "moe_backward_dw",
+           "moe_backward_w", "moe_backward_w_workspace_size"]
 
 
 class MoeForwardOpts(ctypes.Structure):
@@ -84,6 +85,12 @@ _lib.moe_backward_x_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.moe_backward_x_workspace_size.restype = _sz
 _lib.moe_backward_x.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _i, _i, _i, _i, _i, _vp]
 _lib.moe_backward_x.restype = _i
+_lib.moe_backward_dw.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+_lib.moe_backward_dw.restype = _i
+_lib.moe_backward_w_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+_lib.moe_backward_w_workspace_size.restype = _sz
+_lib.moe_backward_w.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _vp]
+_lib.moe_backward_w.restype = _i
 
 
 class MoeError(RuntimeError):
@@ -242,6 +249,30 @@ def moe_backward_x(dgu, dgu_scale, w13_fp8t, w13_s8t, fwd_workspace, dx, k, work
                                _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
                                _ptr(dx), T, d, twoI // 2, E, k, _stream(stream)),
            "moe_backward_x")
+
+
+def moe_backward_dw(dout, fwd_workspace, dw, inter, E, stream=None):
+    """dout bf16 [T, d], fwd_workspace: the forward's workspace; output dw fp32 [T, k]."""
+    T, d = dout.shape
+    k = dw.shape[1]
+    _check(_lib.moe_backward_dw(_ptr(dout), _ptr(fwd_workspace), _ptr(dw), T, d, inter, E, k, _stream(stream)),
+           "moe_backward_dw")
+
+
+def moe_backward_w_workspace_size(T, d, inter, E, k):
+    return _lib.moe_backward_w_workspace_size(T, d, inter, E, k)
+
+
+def moe_backward_w(fwd_workspace, bwd_h_workspace, dgu, dgu_scale, dW13, dW2, k, workspace=None, stream=None):
+    """fwd_workspace: the forward's workspace; bwd_h_workspace: the workspace moe_backward_h was given;
+    dgu, dgu_scale: moe_backward_h's outputs; outputs dW13 fp32 [E, 2*inter, d], dW2 fp32 [E, d, inter]."""
+    E, d, inter = dW2.shape
+    T = dgu.shape[0] // k
+    _check(_lib.moe_backward_w(_ptr(fwd_workspace), _ptr(bwd_h_workspace), _ptr(dgu), _ptr(dgu_scale), _ptr(dW13),
+                               _ptr(dW2), _ptr(workspace),
+                               0 if workspace is None else workspace.numel() * workspace.element_size(),
+                               T, d, inter, E, k, _stream(stream)),
+           "moe_backward_w")
 
 
 def moe_get_device_status(stream=None):

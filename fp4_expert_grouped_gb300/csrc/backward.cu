@@ -130,6 +130,36 @@ __global__ void __launch_bounds__(256) bwd_sf_tiles_kernel(const uint8_t *__rest
     pdl_trigger();
 }
 
+// dw[t][j] = dout[t] . y[pair_pos[t k + j]] (the routing weight's gradient;
+// y is the forward's bf16 expert output, kept in its workspace): one warp per
+// pair, lane l summing channels 8 l .. 8 l + 7 of every 256 in fp32 (each
+// product of two bf16 values exact), then the xor tree.
+__global__ void __launch_bounds__(256) bwd_dw_kernel(const uint16_t *__restrict__ dout, const uint16_t *__restrict__ y,
+                                                     const int32_t *__restrict__ pair_pos, float *__restrict__ dw,
+                                                     long long P, int d, int k)
+{
+    pdl_wait();
+    const long long p = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (p >= P) return;
+    const int lane = threadIdx.x & 31;
+    const uint4 *a = reinterpret_cast<const uint4 *>(dout + (size_t)(p / k) * d);
+    const uint4 *b = reinterpret_cast<const uint4 *>(y + (size_t)__ldg(pair_pos + p) * d);
+    float acc = 0.f;
+    for (int c = lane; c < d / 8; c += 32) {
+        const uint4 u = __ldg(a + c), v = __ldg(b + c);
+        const uint32_t uu[4] = {u.x, u.y, u.z, u.w}, vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            acc = fmaf(bf16_bits_to_f32(uu[i] & 0xFFFFu), bf16_bits_to_f32(vv[i] & 0xFFFFu), acc);
+            acc = fmaf(bf16_bits_to_f32(uu[i] >> 16), bf16_bits_to_f32(vv[i] >> 16), acc);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) dw[p] = acc;
+    pdl_trigger();
+}
+
 namespace {
 
 bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -180,6 +210,11 @@ BwdXLayout bwdx_layout(int T, int d, int inter, int E, int k)
 }
 
 } // namespace
+
+// moe_backward_h's scratch as moe_backward_w reads it: dy's E4M3 codes
+// [P][d] in expert order at offset 0, their scales in the GEMM's tile layout
+size_t bwd_h_dy_offset() { return 0; }
+size_t bwd_h_dys_offset(int T, int d, int inter, int E, int k) { return bwd_layout(T, d, inter, E, k).dys; }
 
 } // namespace fp4moe
 
@@ -355,5 +390,26 @@ extern "C" moe_status moe_backward_x(const uint8_t *dgu, const uint8_t *dgu_scal
         cudaError_t f = cudaFreeAsync(base, s);
         if (e == cudaSuccess) e = f;
     }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status moe_backward_dw(const uint16_t *dout, const void *fwd_workspace, float *dw, int T, int d,
+                                      int inter, int E, int k, void *stream)
+{
+    if (!dout || !fwd_workspace || !dw) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || d <= 0 || inter <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned_to(dout, 16) || !aligned_to(fwd_workspace, 256) || !aligned_to(dw, 4)) return MOE_ERR_INVALID_ARG;
+    Workspace fw;
+    if (!workspace_layout(Shapes{T, d, inter, E, k}, &fw)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    int num_sms = 0;
+    unsigned *status = nullptr;
+    moe_status st = device_query(&num_sms, &status);
+    if (st != MOE_OK) return st;
+    const uint8_t *fb = static_cast<const uint8_t *>(fwd_workspace);
+    const long long P = (long long)T * k;
+    const cudaError_t e = launch_pdl(bwd_dw_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, (cudaStream_t)stream,
+                                     dout, reinterpret_cast<const uint16_t *>(fb + fw.off[MOE_WS_Y]),
+                                     reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_PAIR_POS]), dw, P, d, k);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
         }
         mbar_init(acc_full, 1);
         // small tiles: only the epilogue warps of the lane quarters holding rows
-        mbar_init(acc_empty, C::EPI_Q * 64);
+        mbar_init(acc_empty, C::EPI_Q * 2);       // one arrival per epilogue warp
         for (int i = 0; i < 4; i++) mbar_init(&xbar[i], 64);
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
@@ -530,7 +530,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 tmem_ld32(trow + 128 + 64 * half + 32, u1);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(acc_empty);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
                 if (g.gu_out && r < ti.valid) {
                     // training: keep g and u (fp32) for the backward's SwiGLU
                     float *gd = g.gu_out + row * (2 * (size_t)out_dim) + (size_t)ti.n_block * 128 + 64 * half;
@@ -625,7 +626,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 tmem_ld_wait();
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(acc_empty);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
                 // 32 channels per group: the group's g and u (eight 32-byte loads
                 // per lane, issued together so that one memory round trip
                 // serves the group), then its dh (group 0 from the registers,
@@ -737,7 +739,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 tmem_ld32(trow + 128 * half + 96, v3);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(acc_empty);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
                 if (r < ti.valid) {
                     uint16_t *dst = g.y + row * out_dim + (size_t)ti.n_block * BN + 128 * half;
 #pragma unroll
@@ -761,7 +764,8 @@ __global__ void __launch_bounds__(Cfg<TR>::NUM_THREADS, 1)
                 tmem_ld32(trow + 128 * half + 96, v3);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(acc_empty);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
                 // accumulator half h holds output columns of weight block
                 // n_block + h * ceil(d/256) (the tile's pair of blocks; none for
                 // half 1 of a pair of one block)

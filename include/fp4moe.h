@@ -328,6 +328,51 @@ moe_status moe_backward_h(const uint16_t *dout, const uint8_t *w2_fp8t, const ui
  * Requires d % 256 == 0 and inter % 256 == 0, 1 <= k <= 8, k <= E <= 256.
  * Argument errors are reported before anything is enqueued.
  */
+/*
+ * moe_backward_w -- the master weights' gradients (first page, section 4: the
+ * gradient passes straight through the FP4 quantisation to the FP32 master
+ * weights; section 3.2: fixed summation order).  For every expert e, over its
+ * pairs p in the forward's expert order (ascending pair id: token order, then
+ * slot order), with every operand its E4M3 code times its power-of-two scale:
+ *   dW2[e]  = sum_p dy_p (x) h_p          fp32 [E][d][inter]
+ *   dW13[e] = sum_p [dg; du]_p (x) x_p    fp32 [E][2*inter][d]
+ * (dy_p as moe_backward_h quantised it, h_p and x_p as the forward's GEMMs read
+ * them, [dg; du]_p as moe_backward_h wrote it).  The operands are dequantised to
+ * bf16 (exact for E4M3 times a power of two within bf16's range) and the sums
+ * run on the bf16 tensor cores in fp32, in pair order.  Experts without pairs
+ * get zero gradients.
+ *   fwd_workspace     device, the forward call's workspace (plan, xq, hq and scales)
+ *   bwd_h_workspace   device, the workspace moe_backward_h was given (its dy
+ *                     codes and scales are read; moe_backward_h must have been
+ *                     called with a caller workspace, not NULL)
+ *   dgu, dgu_scale    device, moe_backward_h's outputs, dgu 16-byte aligned
+ *   dW13, dW2         device, fp32 outputs, 32-byte aligned
+ *   workspace         device scratch of moe_backward_w_workspace_size bytes,
+ *                     256-byte aligned, or NULL (then allocated stream-ordered)
+ * Requires d % 256 == 0 and inter % 256 == 0, 1 <= k <= 8, k <= E <= 256.
+ * Argument errors are reported before anything is enqueued.
+ */
+size_t moe_backward_w_workspace_size(int T, int d, int inter, int E, int k);
+moe_status moe_backward_w(const void *fwd_workspace, const void *bwd_h_workspace, const uint8_t *dgu,
+                          const uint8_t *dgu_scale, float *dW13, float *dW2, void *workspace, size_t workspace_bytes,
+                          int T, int d, int inter, int E, int k, void *stream);
+
+/*
+ * moe_backward_dw -- the gradient with respect to the routing weights (the
+ * backward of the weighted combine, first page section 1.4): for every pair
+ * p = t*k + j, dw[p] = sum over c of dout[t][c] * y_p[c], y_p the pair's bf16
+ * expert output that the forward kept in its workspace (fp32 sum, lane-strided
+ * partial sums and a fixed tree; deterministic).  Routing is held fixed: the
+ * gate's own backward is the caller's.
+ *   dout           device, bf16 [T][d], 16-byte aligned
+ *   fwd_workspace  device, the forward call's workspace (y and the plan are read)
+ *   dw             device, fp32 [T][k]
+ * Requires the forward's shapes.  Argument errors are reported before
+ * anything is enqueued.
+ */
+moe_status moe_backward_dw(const uint16_t *dout, const void *fwd_workspace, float *dw, int T, int d, int inter, int E,
+                           int k, void *stream);
+
 size_t moe_backward_x_workspace_size(int T, int d, int inter, int E, int k);
 moe_status moe_backward_x(const uint8_t *dgu, const uint8_t *dgu_scale, const uint8_t *w13_fp8t,
                           const uint8_t *w13_s8t, const void *fwd_workspace, void *workspace, size_t workspace_bytes,

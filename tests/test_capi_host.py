@@ -162,3 +162,26 @@ def test_backward_x_argument_checks(capi):
     assert lib.moe_backward_x(F, F, F, F, F, None, 0, F, 0, 256, 256, 8, 2, None) == 0      # T == 0: no-op
     assert capi.moe_backward_x_workspace_size(8, 256, 384, 8, 2) == 0
     assert capi.moe_backward_x_workspace_size(8, 256, 256, 8, 2) > 0
+
+
+def test_backward_dw_argument_checks(capi):
+    """moe_backward_dw rejects bad shapes and pointers before touching CUDA."""
+    lib = capi.lib()
+    F = 0x100000
+    assert lib.moe_backward_dw(F, F, None, 8, 256, 256, 8, 2, None) == 1       # no output
+    assert lib.moe_backward_dw(F + 8, F, F, 8, 256, 256, 8, 2, None) == 1      # dout alignment
+    assert lib.moe_backward_dw(F, F, F, 8, 320, 256, 8, 2, None) == 2          # d % 128
+    assert lib.moe_backward_dw(F, F, F, 0, 256, 256, 8, 2, None) == 0          # T == 0: no-op
+
+
+def test_backward_w_argument_checks(capi):
+    """moe_backward_w rejects bad shapes and pointers before touching CUDA."""
+    lib = capi.lib()
+    F = 0x100000
+    assert lib.moe_backward_w(F, F, F, F, F, F, None, 0, 8, 256, 384, 8, 2, None) == 2      # inter % 256
+    assert lib.moe_backward_w(F, F, F, F, F, F, None, 0, 8, 384, 256, 8, 2, None) == 2      # d % 256
+    assert lib.moe_backward_w(F, None, F, F, F, F, None, 0, 8, 256, 256, 8, 2, None) == 1   # no dy source
+    assert lib.moe_backward_w(F, F, F, F, F + 16, F, None, 0, 8, 256, 256, 8, 2, None) == 1  # dW13 alignment
+    assert lib.moe_backward_w(F, F, F, F, F, F, F, 16, 8, 256, 256, 8, 2, None) == 4        # workspace too small
+    assert capi.moe_backward_w_workspace_size(8, 256, 384, 8, 2) == 0
+    assert capi.moe_backward_w_workspace_size(8, 256, 256, 8, 2) > 0

@@ -68,7 +68,8 @@ def run_backward(T, d, inter, E, k, seed, bias=False):
     dgu = torch.empty((T * k, 2 * inter), dtype=torch.uint8, device=DEV)
     dgs = torch.empty((T * k, 2 * inter // 128), dtype=torch.uint8, device=DEV)
     dgf = torch.empty((T * k, 2 * inter), dtype=torch.float32, device=DEV)
-    c.moe_backward_h(dout.to(DEV), w8, s8, gu, ws, dgu, dgs, k, dgu_f32=dgf)
+    bws = torch.empty(c.moe_backward_h_workspace_size(T, d, inter, E, k), dtype=torch.uint8, device=DEV)
+    c.moe_backward_h(dout.to(DEV), w8, s8, gu, ws, dgu, dgs, k, dgu_f32=dgf, workspace=bws)
     assert c.moe_get_device_status() == 0
     again = torch.empty_like(dgu)
     again_s = torch.empty_like(dgs)
@@ -83,10 +84,21 @@ def run_backward(T, d, inter, E, k, seed, bias=False):
     dx2 = torch.empty_like(dx)
     c.moe_backward_x(dgu, dgs, w8x, s8x, ws, dx2, k)
     assert torch.equal(dx, dx2)                                          # deterministic
+    dw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    c.moe_backward_dw(dout.to(DEV), ws, dw, inter, E)
+    # the master weights' gradients
+    dW13 = torch.full((E, 2 * inter, d), float("nan"), dtype=torch.float32, device=DEV)
+    dW2 = torch.full((E, d, inter), float("nan"), dtype=torch.float32, device=DEV)
+    c.moe_backward_w(ws, bws, dgu, dgs, dW13, dW2, k)
+    dW2b = torch.empty_like(dW2)
+    dW13b = torch.empty_like(dW13)
+    c.moe_backward_w(ws, bws, dgu, dgs, dW13b, dW2b, k)
+    assert torch.equal(dW2, dW2b) and torch.equal(dW13, dW13b)          # deterministic
     assert c.moe_get_device_status() == 0
     return dict(x=x, gw=gw, b=b, w13=w13, w2=w2, ti=ti.cpu().numpy(), pp=pp.cpu().numpy(), wts=wts.numpy(),
                 dout=dout, dgu=dgu.cpu().numpy(), dgs=dgs.cpu().numpy(), dgf=dgf.cpu().numpy().astype(np.float64),
-                dx=inputs.bf16_bits(dx.cpu()))
+                dx=inputs.bf16_bits(dx.cpu()), dw=dw.cpu().numpy().astype(np.float64),
+                dW13=dW13.cpu().numpy().astype(np.float64), dW2=dW2.cpu().numpy().astype(np.float64))
 
 
 def oracle_routing(r, E, k):
@@ -138,14 +150,38 @@ def check_against_oracle(r, T, d, inter, E, k, pairs=None):
 
 
 def check_dx_against_oracle(r, T, d, inter, E, k):
-    """dx of every token against the oracle's backward step (its own routing, the
-    test's routing weights, quantised gradients) at the layer tolerance."""
+    """dx of every token, dw of every pair and the master weights' gradients dW2,
+    dW13 of every expert against the oracle's backward step (its own routing,
+    the test's routing weights, quantised gradients) at the layer tolerance."""
     xb = inputs.bf16_bits(r["x"])
     f13, s13 = oracle.pack_fp4(r["w13"].numpy())
     f2, s2 = oracle.pack_fp4(r["w2"].numpy())
     ti, _ = oracle_routing(r, E, k)
     tw = np.tile(r["wts"], (T, 1)).astype(np.float32)
-    ref, _, _, _ = qat.qat_backward(xb, ti, tw, f13, s13, f2, s2, inputs.bf16_bits(r["dout"]), quantize_grads=True)
+    ref, ref_dw, ref_dW13, ref_dW2 = qat.qat_backward(xb, ti, tw, f13, s13, f2, s2, inputs.bf16_bits(r["dout"]),
+                                                      quantize_grads=True)
+    # the master weights' gradients: exact zeros for experts without pairs; the
+    # layer tolerance over each whole tensor; and per expert with at least 8
+    # pairs.  (An expert with one or two pairs shows a single [dg; du] code that
+    # the GPU's fp32 and the oracle's float64 round to neighbouring E4M3 values,
+    # one step, as a whole row of its gradient: the per-pair comparison above
+    # bounds how many such codes there are.)
+    n_e = np.bincount(ti.reshape(-1), minlength=E)
+    for name, got_w, ref_w in (("dW2", r["dW2"], ref_dW2), ("dW13", r["dW13"], ref_dW13)):
+        assert np.all(np.isfinite(got_w)), name
+        for e in range(E):
+            if n_e[e] == 0:
+                assert not np.any(got_w[e]) and not np.any(ref_w[e]), (name, e)
+        assert np.abs(got_w - ref_w).max() <= 1e-2 * np.abs(ref_w).max(), (name, np.abs(got_w - ref_w).max())
+        assert np.linalg.norm(got_w - ref_w) <= 5e-3 * np.linalg.norm(ref_w), name
+        for e in np.nonzero(n_e >= 8)[0]:
+            g_e, r_e = got_w[e], ref_w[e]
+            assert np.abs(g_e - r_e).max() <= 1e-2 * np.abs(r_e).max(), (name, e, np.abs(g_e - r_e).max())
+            assert np.linalg.norm(g_e - r_e) <= 5e-3 * np.linalg.norm(r_e), (name, e)
+    # dw = dout . y per pair (y: each side's own bf16 expert output)
+    dwe = np.abs(r["dw"] - ref_dw)
+    assert dwe.max() <= 1e-2 * np.abs(ref_dw).max(), (dwe.max(), np.abs(ref_dw).max())
+    assert np.linalg.norm(r["dw"] - ref_dw) <= 5e-3 * np.linalg.norm(ref_dw)
     got = (r["dx"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     err = np.abs(got - ref)
     assert err.max() <= 1e-2 * np.abs(ref).max(), (err.max(), np.abs(ref).max())
@@ -159,6 +195,7 @@ def check_dx_against_oracle(r, T, d, inter, E, k):
     (150, 256, 256, 8, 2, False),          # 64-row tiles
     (700, 256, 512, 8, 2, True),           # 128-row tiles, two 256-channel blocks of dh
     (64, 256, 256, 4, 4, False),           # k == E
+    (10, 256, 512, 32, 2, False),          # most experts without pairs: zero weight gradients
 ])
 def test_backward_matches_oracle(T, d, inter, E, k, bias):
     r = run_backward(T, d, inter, E, k, seed=T + d, bias=bias)
