@@ -409,9 +409,12 @@ constexpr int kCertWarps = 4;           // tokens per CTA (a warp each)
 // The fixed-order logits of GS candidate experts ec[0..GS) of one token, by
 // one warp: lane l runs chain l (channels l, l+32, ... with fused
 // multiply-adds), the xor tree adds the chains in the fixed order's pairs, the
-// bias comes last; the result goes to the lane holding that expert.  Eight
-// channel steps of all GS experts' weights are loaded before their
-// multiply-adds, so each lane has up to 8 GS loads in flight.
+// bias comes last; the result goes to the lane holding that expert.  U channel
+// steps of all GS experts' weights (and of x) are loaded before their
+// multiply-adds: U = 8 for a group of 8, more for the smaller groups that take
+// the last candidates (32 for one, 16 for two or four), so that every group
+// keeps about 70 loads per lane in flight (the step is latency-bound: a group
+// of one at U = 8 took as long as a group of eight).
 template <int GS>
 __device__ __forceinline__ void exact_logits(const int *ec_list, const uint16_t *__restrict__ xrow,
                                              const float *__restrict__ wt, const float *__restrict__ bias, int d,
@@ -429,8 +432,22 @@ __device__ __forceinline__ void exact_logits(const int *ec_list, const uint16_t 
 #pragma unroll
     for (int c = 0; c < GS; c++) acc[c] = 0.f;
     const int nj = d / 32;
+    constexpr int U = GS == 1 ? 32 : GS <= 4 ? 16 : 8;
     int j = 0;
-    for (; j + 8 <= nj; j += 8) {
+    for (; j + U <= nj; j += U) {
+        float xv[U], wv[GS][U];
+#pragma unroll
+        for (int u = 0; u < U; u++) xv[u] = bf16_bits_to_f32(__ldg(xp + (j + u) * 32));
+#pragma unroll
+        for (int c = 0; c < GS; c++)
+#pragma unroll
+            for (int u = 0; u < U; u++) wv[c][u] = __ldg(wp[c] + (j + u) * 32);
+#pragma unroll
+        for (int u = 0; u < U; u++)
+#pragma unroll
+            for (int c = 0; c < GS; c++) acc[c] = fmaf(xv[u], wv[c][u], acc[c]);
+    }
+    for (; j + 8 <= nj; j += 8) {             // what is left of the U-step blocks, 8 steps at a time
         float xv[8], wv[GS][8];
 #pragma unroll
         for (int u = 0; u < 8; u++) xv[u] = bf16_bits_to_f32(__ldg(xp + (j + u) * 32));
