@@ -223,14 +223,15 @@ def gemm_flops(w, which):
 GATE_TC_MIN_TOKENS = 1024      # the library's tensor-core gate threshold (include/fp4moe.h)
 
 
-def kernels_per_step(w):
+def kernels_per_step(w, gate_prepared=True):
     """Kernels the library launches for one forward of workload w: the gate
     and top-k (two kernels below 1024 tokens; from there, with E a multiple of
-    64, four: gate_w split, weight norms, tensor-core logits, certified
-    top-k), the dispatch plan (a count and a scatter kernel beyond 32768
-    pairs, one kernel up to that), the expert-ordered copy (from 16 pairs per
-    expert on average), GEMM1, GEMM2, combine."""
-    gate = 4 if w.T >= GATE_TC_MIN_TOKENS and w.E % 64 == 0 else 2
+    64, the tensor-core logits and the certified top-k, plus gate_w's split
+    and weight norms unless prepared at load time), the dispatch plan (a count
+    and a scatter kernel beyond 32768 pairs, one kernel up to that), the
+    expert-ordered copy (from 16 pairs per expert on average), GEMM1, GEMM2,
+    combine."""
+    gate = (2 if gate_prepared else 4) if w.T >= GATE_TC_MIN_TOKENS and w.E % 64 == 0 else 2
     plan = 2 if w.P > 32768 else 1
     dispatch = 1 if w.P >= 16 * w.E else 0
     return gate + plan + dispatch + 3
@@ -333,6 +334,7 @@ def run_reference(args, w, ws_, rank):
 def config_of(w):
     return {"workload": w.name, "T": w.T, "d": w.d, "inter": w.inter, "E": w.E, "k": w.k,
             "zipf_bias": w.zipf_bias, "seed": w.seed,
+            "weights": "experts packed to MXFP4 and gate_w prepared for the tensor-core gate at load time",
             "l2": "flushed (256 MiB write) before every timed step; weights %.2f GB >> 129 MB L2"
                   % (w.E * weight_bytes_per_expert(w.d, w.inter) / 1e9)}
 
@@ -349,6 +351,9 @@ def run_ours(args, w, world, rank, local):
     x, gw, bias = inputs.make_x_gate(w, dev)
     pk = layer.pack_workload(w, dev)
     ws = layer.workspace(w.T, w.d, w.inter, w.E, w.k, dev)
+    # gate_w's form for the tensor-core gate, prepared at load time like the
+    # packed experts (a function of the weights only)
+    gprep = layer.prepare_gate(gw)
     out = torch.empty_like(x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -362,7 +367,7 @@ def run_ours(args, w, world, rank, local):
 
     def step(evs):
         capi.moe_forward_ex(x, gw, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, out, w.k,
-                            stream=stream, gate_bias=bias, workspace=ws, stage_events=evs)
+                            stream=stream, gate_bias=bias, workspace=ws, stage_events=evs, gate_prep=gprep)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -434,7 +439,7 @@ def run_ours(args, w, world, rank, local):
         step(None)
         out_host.copy_(out, non_blocking=True)
 
-    graphed = layer.GraphedForward(x_host, gw, pk, w.k, gate_bias=bias)
+    graphed = layer.GraphedForward(x_host, gw, pk, w.k, gate_bias=bias, gate_prep=gprep)
 
     def time_e2e(run):
         for _ in range(2):
@@ -458,7 +463,7 @@ def run_ours(args, w, world, rank, local):
         raise RuntimeError("graphed and eager steps disagree")
     del graphed
 
-    pipe = layer.PipelinedForward(w.T, w.d, gw, pk, w.k, gate_bias=bias, stream=stream)
+    pipe = layer.PipelinedForward(w.T, w.d, gw, pk, w.k, gate_bias=bias, stream=stream, gate_prep=gprep)
     pipe_out = torch.empty_like(out_host).pin_memory()
     for _ in range(2):
         pipe.step(x_host, pipe_out)

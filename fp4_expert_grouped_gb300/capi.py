@@ -38,7 +38,7 @@ EXPORTS = ["moe_status_string", "moe_version", "moe_pack_fp4", "moe_fp4_to_fp8t"
            "moe_route_noalloc", "moe_dispatch_plan", "moe_forward", "moe_forward_ex", "moe_workspace_size",
            "moe_workspace_layout", "moe_get_device_status", "moe_backward_h", "moe_backward_h_workspace_size",
            "moe_backward_x", "moe_backward_x_workspace_size", "moe_backward_dw",
-           "moe_backward_w", "moe_backward_w_workspace_size"]
+           "moe_backward_w", "moe_backward_w_workspace_size", "moe_gate_prep_size", "moe_prepare_gate"]
 
 
 class MoeForwardOpts(ctypes.Structure):
@@ -46,7 +46,7 @@ class MoeForwardOpts(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("topk_idx_out", ctypes.c_void_p),
                 ("topk_w_out", ctypes.c_void_p), ("pair_pos_out", ctypes.c_void_p),
                 ("flags", ctypes.c_uint32), ("stage_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("gu_out", ctypes.c_void_p)]
+                ("gu_out", ctypes.c_void_p), ("gate_prep", ctypes.c_void_p)]
 
 
 _vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -91,6 +91,10 @@ _lib.moe_backward_w_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.moe_backward_w_workspace_size.restype = _sz
 _lib.moe_backward_w.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _vp]
 _lib.moe_backward_w.restype = _i
+_lib.moe_gate_prep_size.argtypes = [_i, _i]
+_lib.moe_gate_prep_size.restype = _sz
+_lib.moe_prepare_gate.argtypes = [_vp, _vp, _i, _i, _vp]
+_lib.moe_prepare_gate.restype = _i
 
 
 class MoeError(RuntimeError):
@@ -199,7 +203,7 @@ def moe_forward(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stream=
 
 def moe_forward_ex(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stream=None, gate_bias=None,
                    workspace=None, topk_idx_out=None, topk_w_out=None, pair_pos_out=None, flags=0,
-                   stage_events=None, gu_out=None):
+                   stage_events=None, gu_out=None, gate_prep=None):
     """stage_events: optional list of len(STAGES) + 1 recorded torch.cuda.Event objects."""
     T, d = x.shape
     E = gate_w.shape[1]
@@ -212,10 +216,20 @@ def moe_forward_ex(x, gate_w, w13_fp4, w13_scale, w2_fp4, w2_scale, out, k, stre
                        0 if workspace is None else workspace.numel() * workspace.element_size(),
                        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(pair_pos_out), flags,
                        ctypes.cast(evs, ctypes.POINTER(ctypes.c_void_p)) if evs is not None else None,
-                       _ptr(gu_out))
+                       _ptr(gu_out), _ptr(gate_prep))
     _check(_lib.moe_forward_ex(_ptr(x), _ptr(gate_w), _ptr(w13_fp4), _ptr(w13_scale), _ptr(w2_fp4),
                                _ptr(w2_scale), _ptr(out), T, d, inter, E, k, _stream(stream),
                                ctypes.byref(o)), "moe_forward_ex")
+
+
+def moe_gate_prep_size(d, E):
+    return _lib.moe_gate_prep_size(d, E)
+
+
+def moe_prepare_gate(gate_w, prep, stream=None):
+    """gate_w fp32 [d, E] -> prep (uint8, moe_gate_prep_size(d, E) bytes): the tensor-core gate's form of it."""
+    d, E = gate_w.shape
+    _check(_lib.moe_prepare_gate(_ptr(gate_w), _ptr(prep), d, E, _stream(stream)), "moe_prepare_gate")
 
 
 def moe_backward_h_workspace_size(T, d, inter, E, k):

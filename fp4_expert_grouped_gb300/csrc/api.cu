@@ -236,6 +236,7 @@ moe_status moe_route(const uint16_t *x, const float *gate_w, const float *gate_b
         g.wlo = reinterpret_cast<uint16_t *>(b + zb + wtb + wpb);
         g.wn = reinterpret_cast<float *>(b + zb + wtb + 2 * wpb);
         g.ncand = reinterpret_cast<int32_t *>(b + zb + wtb + 2 * wpb + wnb);
+        g.prepared = false;
         e = launch_gate_tc_logits(x, gate_w, gate_bias, g, T, d, E, di->num_sms, di->status, timeout_ns(), s);
         if (e == cudaSuccess)
             e = launch_gate_certify(x, gate_bias, g, topk_idx, topk_w, nullptr, nullptr, nullptr, 0, T, d, E, k,
@@ -285,6 +286,32 @@ size_t moe_workspace_layout(int T, int d, int inter, int E, int k, size_t *offse
     return ws.total;
 }
 
+size_t moe_gate_prep_size(int d, int E)
+{
+    if (d <= 0 || E <= 0 || d % 128 || E > 256) return 0;
+    return gate_prep_layout(d, E).total;
+}
+
+moe_status moe_prepare_gate(const float *gate_w, void *prep, int d, int E, void *stream)
+{
+    if (!gate_w || !prep || !aligned(gate_w, 16) || !aligned(prep, 256)) return MOE_ERR_INVALID_ARG;
+    if (d <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    if (d % 128 || E > 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+    int num_sms = 0;
+    unsigned *status = nullptr;
+    moe_status st = device_query(&num_sms, &status);
+    if (st != MOE_OK) return st;
+    const GatePrepLayout gl = gate_prep_layout(d, E);
+    uint8_t *gp = static_cast<uint8_t *>(prep);
+    GateScratch g;
+    std::memset(&g, 0, sizeof g);
+    g.wt = reinterpret_cast<float *>(gp + gl.wt);
+    g.whi = reinterpret_cast<uint16_t *>(gp + gl.whi);
+    g.wlo = reinterpret_cast<uint16_t *>(gp + gl.wlo);
+    g.wn = reinterpret_cast<float *>(gp + gl.wn);
+    return launch_gate_prep(gate_w, g, d, E, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 size_t moe_workspace_size(int T, int d, int inter, int E, int k)
 {
     return moe_workspace_layout(T, d, inter, E, k, nullptr, nullptr);
@@ -305,7 +332,8 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
     if (o.flags & ~MOE_FLAG_TEST_STALL_GEMM2) return MOE_ERR_INVALID_ARG;
     if (o.gate_bias && !aligned(o.gate_bias, 4)) return MOE_ERR_INVALID_ARG;
     if ((o.topk_idx_out && !aligned(o.topk_idx_out, 4)) || (o.topk_w_out && !aligned(o.topk_w_out, 4)) ||
-        (o.pair_pos_out && !aligned(o.pair_pos_out, 4)) || (o.gu_out && !aligned(o.gu_out, 32)))
+        (o.pair_pos_out && !aligned(o.pair_pos_out, 4)) || (o.gu_out && !aligned(o.gu_out, 32)) ||
+        (o.gate_prep && !aligned(o.gate_prep, 256)))
         return MOE_ERR_INVALID_ARG;
     if (!layer_shape_ok(T, d, inter, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
     Workspace ws;
@@ -353,10 +381,21 @@ moe_status moe_forward_ex(const uint16_t *x, const float *gate_w, const uint8_t 
         // tensor-core logits, then (the top-k stage) the certified top-k with
         // the candidates' fixed-order logits and the FP8 quantisation of x
         GateScratch gs;
-        gs.wt = reinterpret_cast<float *>(at(MOE_WS_GATE_WT));
-        gs.whi = reinterpret_cast<uint16_t *>(at(MOE_WS_GATE_WHI));
-        gs.wlo = reinterpret_cast<uint16_t *>(at(MOE_WS_GATE_WLO));
-        gs.wn = reinterpret_cast<float *>(at(MOE_WS_GATE_WNORM));
+        if (o.gate_prep) {                      // gate_w's split and norms, prepared at load time
+            const GatePrepLayout gl = gate_prep_layout(d, E);
+            uint8_t *gp = static_cast<uint8_t *>(const_cast<void *>(o.gate_prep));
+            gs.wt = reinterpret_cast<float *>(gp + gl.wt);
+            gs.whi = reinterpret_cast<uint16_t *>(gp + gl.whi);
+            gs.wlo = reinterpret_cast<uint16_t *>(gp + gl.wlo);
+            gs.wn = reinterpret_cast<float *>(gp + gl.wn);
+            gs.prepared = true;
+        } else {
+            gs.wt = reinterpret_cast<float *>(at(MOE_WS_GATE_WT));
+            gs.whi = reinterpret_cast<uint16_t *>(at(MOE_WS_GATE_WHI));
+            gs.wlo = reinterpret_cast<uint16_t *>(at(MOE_WS_GATE_WLO));
+            gs.wn = reinterpret_cast<float *>(at(MOE_WS_GATE_WNORM));
+            gs.prepared = false;
+        }
         gs.approx = logits;
         gs.ncand = reinterpret_cast<int32_t *>(at(MOE_WS_GATE_NCAND));
         if (e == cudaSuccess)

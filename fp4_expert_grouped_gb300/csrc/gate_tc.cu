@@ -337,13 +337,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // The token's bf16 row, 8 channels per lane and step, quantised to E4M3 with
 // one power-of-two scale per 128 channels when qrow is given (two groups per
 // step, one per half-warp: the rule of moe_quantize_act); returns this lane's
-// part of the row's sum of squares.  The row is read eight steps (8 KB) at a
+// part of the row's sum of squares.  The row is read B steps (B KB) at a
 // time, all loads in flight together: the row comes from DRAM, and one
-// dependent load per step made this the longest part of a token's work.
+// dependent load per step made this the longest part of a token's work.  B =
+// 8 up to d = 4096 (two batches), 12 above (three batches instead of four at
+// d = 7168: certify 349 -> 326 us at 16K tokens; at d = 4096 the larger batch
+// only cost registers).
+template <int B>
 __device__ __forceinline__ float quant_row_ssq(const uint16_t *__restrict__ xrow, uint8_t *__restrict__ qrow,
                                                uint8_t *__restrict__ srow, int d, int s_stride)
 {
-    constexpr int B = 8;
     const int lane = threadIdx.x & 31;
     const int n8 = d / 8;
     const uint4 *src = reinterpret_cast<const uint4 *>(xrow);
@@ -484,6 +487,7 @@ __device__ __forceinline__ void exact_logits(const int *ec_list, const uint16_t 
     }
 }
 
+template <int QB>
 __global__ void __launch_bounds__(kCertWarps * 32) gate_certify_kernel(
     const uint16_t *__restrict__ x, const float *__restrict__ approx, const float *__restrict__ wt,
     const float *__restrict__ wn, const float *__restrict__ bias, float crel, int32_t *__restrict__ topk_idx,
@@ -498,7 +502,7 @@ __global__ void __launch_bounds__(kCertWarps * 32) gate_certify_kernel(
     int *cl = reinterpret_cast<int *>(cert_smem) + warp * 256;     // the token's candidates
 
     // the row, its quantisation and an upper bound of ||x||_2 (as for the weights)
-    float ssq = quant_row_ssq(x + (size_t)t * d, xq ? xq + (size_t)t * d : nullptr,
+    float ssq = quant_row_ssq<QB>(x + (size_t)t * d, xq ? xq + (size_t)t * d : nullptr,
                               xq ? xs + (size_t)t * xs_stride : nullptr, d, xs_stride);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) ssq = ssq + __shfl_xor_sync(0xffffffffu, ssq, off);
@@ -713,17 +717,25 @@ static cudaError_t launch_gate_tc_cfg(const CUtensorMap &mx, const CUtensorMap &
                       status, timeout_ns);
 }
 
+cudaError_t launch_gate_prep(const float *gate_w, const GateScratch &g, int d, int E, cudaStream_t st)
+{
+    cudaError_t err = launch_pdl(gate_split_kernel, dim3(d / 32, (E + 31) / 32), dim3(256), 0, st, gate_w, g.wt, g.whi,
+                                 g.wlo, d, E);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(gate_wnorm_kernel, dim3((E + 7) / 8), dim3(256), 0, st, (const float *)g.wt, g.wn, d, E);
+}
+
 cudaError_t launch_gate_tc_logits(const uint16_t *x, const float *gate_w, const float *bias, const GateScratch &g,
                                   int T, int d, int E, int num_sms, unsigned *status, unsigned long long timeout_ns,
                                   cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
     if (!gate_uses_tc(T, d, E)) return cudaErrorInvalidValue;
-    cudaError_t err = launch_pdl(gate_split_kernel, dim3(d / 32, (E + 31) / 32), dim3(256), 0, st, gate_w, g.wt,
-                                 g.whi, g.wlo, d, E);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(gate_wnorm_kernel, dim3((E + 7) / 8), dim3(256), 0, st, (const float *)g.wt, g.wn, d, E);
-    if (err != cudaSuccess) return err;
+    cudaError_t err = cudaSuccess;
+    if (!g.prepared) {
+        err = launch_gate_prep(gate_w, g, d, E, st);
+        if (err != cudaSuccess) return err;
+    }
     CUtensorMap mx, mh, ml;
     if (!make_map_bf16(&mx, x, T, d, gtc::BM) || !make_map_bf16(&mh, g.whi, E, d, E) ||
         !make_map_bf16(&ml, g.wlo, E, d, E))
@@ -743,9 +755,10 @@ cudaError_t launch_gate_certify(const uint16_t *x, const float *bias, const Gate
 {
     if (T == 0) return cudaSuccess;
     const size_t smem = (size_t)kCertWarps * 256 * 4;
-    cudaError_t err = cudaFuncSetAttribute(gate_certify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = d > 4096 ? gate_certify_kernel<12> : gate_certify_kernel<8>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(gate_certify_kernel, dim3((T + kCertWarps - 1) / kCertWarps), dim3(kCertWarps * 32), smem, st,
+    return launch_pdl(kern, dim3((T + kCertWarps - 1) / kCertWarps), dim3(kCertWarps * 32), smem, st,
                       x, (const float *)g.approx, (const float *)g.wt, (const float *)g.wn, bias,
                       gate_bound_coefficient(d), topk_idx, topk_w, topk_z, g.ncand, xq, xs, xs_stride, T, d, E, k,
                       status);

@@ -190,7 +190,25 @@ struct GateScratch {
     float *wn;          // fp32 [E]: upper bounds of the experts' weight norms
     float *approx;      // fp32 [T][E]: tensor-core logits (+ bias)
     int32_t *ncand;     // int32 [T]: candidate experts per token (or NULL)
+    bool prepared;      // wt, whi, wlo, wn already hold gate_w's (moe_prepare_gate)
 };
+// gate_w's transposed fp32 rows, bf16 split and weight norms into g
+cudaError_t launch_gate_prep(const float *gate_w, const GateScratch &g, int d, int E, cudaStream_t st);
+// where moe_prepare_gate puts them in its buffer
+struct GatePrepLayout {
+    size_t wt, whi, wlo, wn, total;
+};
+inline GatePrepLayout gate_prep_layout(int d, int E)
+{
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    GatePrepLayout l;
+    l.wt = 0;
+    l.whi = up((size_t)E * d * 4);
+    l.wlo = l.whi + up((size_t)E * d * 2);
+    l.wn = l.wlo + up((size_t)E * d * 2);
+    l.total = l.wn + up((size_t)E * 4);
+    return l;
+}
 // the tensor-core logits: gate_w split and transposed, the weight norms, then
 // g.approx = x . (hi + lo) + bias
 cudaError_t launch_gate_tc_logits(const uint16_t *x, const float *gate_w, const float *bias, const GateScratch &g,

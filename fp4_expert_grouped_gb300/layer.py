@@ -57,10 +57,18 @@ def workspace(T: int, d: int, inter: int, E: int, k: int, device="cuda") -> torc
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
+def prepare_gate(gate_w: torch.Tensor) -> torch.Tensor:
+    """gate_w's form for the tensor-core gate (moe_prepare_gate), once per gate_w."""
+    d, E = gate_w.shape
+    prep = torch.empty(max(capi.moe_gate_prep_size(d, E), 256), dtype=torch.uint8, device=gate_w.device)
+    capi.moe_prepare_gate(gate_w, prep)
+    return prep
+
+
 def forward(x: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
             gate_bias: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
             out: Optional[torch.Tensor] = None, stream=None, routing: bool = False,
-            gu_out: Optional[torch.Tensor] = None):
+            gu_out: Optional[torch.Tensor] = None, gate_prep: Optional[torch.Tensor] = None):
     """out bf16 [T, d] = MoE layer forward of bf16 x [T, d] (device tensors).
     With routing=True also returns (topk_idx, topk_w, pair_pos).  gu_out (fp32
     [T*k, 2*inter]) keeps GEMM1's g and u for the backward (moe_backward_h)."""
@@ -74,7 +82,7 @@ def forward(x: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
         pp = torch.empty((T * k,), dtype=torch.int32, device=x.device)
     capi.moe_forward_ex(x, gate_w, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, out, k,
                         stream=stream, gate_bias=gate_bias, workspace=ws,
-                        topk_idx_out=ti, topk_w_out=tw, pair_pos_out=pp, gu_out=gu_out)
+                        topk_idx_out=ti, topk_w_out=tw, pair_pos_out=pp, gu_out=gu_out, gate_prep=gate_prep)
     if routing:
         return out, ti, tw, pp
     return out
@@ -99,7 +107,8 @@ class GraphedForward:
     """
 
     def __init__(self, x_host: torch.Tensor, gate_w: torch.Tensor, pk: PackedExperts, k: int,
-                 gate_bias: Optional[torch.Tensor] = None, out_host: Optional[torch.Tensor] = None):
+                 gate_bias: Optional[torch.Tensor] = None, out_host: Optional[torch.Tensor] = None,
+                 gate_prep: Optional[torch.Tensor] = None):
         if not x_host.is_pinned():
             raise ValueError("x_host must be pinned host memory")
         dev = gate_w.device
@@ -113,7 +122,7 @@ class GraphedForward:
         self.x = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
         self.out = torch.empty_like(self.x)
         self.ws = workspace(T, d, inter, E, k, dev)
-        self._args = (gate_w, pk, k, gate_bias)
+        self._args = (gate_w, pk, k, gate_bias, gate_prep)
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
@@ -126,9 +135,9 @@ class GraphedForward:
             self._forward()
 
     def _forward(self):
-        gate_w, pk, k, gate_bias = self._args
+        gate_w, pk, k, gate_bias, gate_prep = self._args
         capi.moe_forward_ex(self.x, gate_w, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, self.out, k,
-                            gate_bias=gate_bias, workspace=self.ws)
+                            gate_bias=gate_bias, workspace=self.ws, gate_prep=gate_prep)
 
     def replay(self):
         """Enqueue one step on the current stream."""
@@ -153,7 +162,8 @@ class PipelinedForward:
     """
 
     def __init__(self, T: int, d: int, gate_w: torch.Tensor, pk: PackedExperts, k: int,
-                 gate_bias: Optional[torch.Tensor] = None, depth: int = 2, stream=None):
+                 gate_bias: Optional[torch.Tensor] = None, depth: int = 2, stream=None,
+                 gate_prep: Optional[torch.Tensor] = None):
         if depth < 1:
             raise ValueError("depth must be at least 1")
         dev = gate_w.device
@@ -170,14 +180,14 @@ class PipelinedForward:
         self.fwd_done = [torch.cuda.Event() for _ in range(depth)]
         self.out_done = [torch.cuda.Event() for _ in range(depth)]
         self._used = [False] * depth
-        self._args = (gate_w, pk, k, gate_bias)
+        self._args = (gate_w, pk, k, gate_bias, gate_prep)
         self.i = 0
         self.in_event = None
 
     def step(self, x_host: torch.Tensor, out_host: torch.Tensor) -> torch.cuda.Event:
         if not (x_host.is_pinned() and out_host.is_pinned()):
             raise ValueError("x_host and out_host must be pinned host memory")
-        gate_w, pk, k, gate_bias = self._args
+        gate_w, pk, k, gate_bias, gate_prep = self._args
         s = self.i % self.depth
         if self._used[s]:
             self.h2d.wait_event(self.fwd_done[s])          # the forward that read x[s] is done
@@ -188,7 +198,7 @@ class PipelinedForward:
         if self._used[s]:
             self.compute.wait_event(self.out_done[s])      # the copy-out that read out[s] is done
         capi.moe_forward_ex(self.x[s], gate_w, pk.w13_fp4, pk.w13_scale, pk.w2_fp4, pk.w2_scale, self.out[s], k,
-                            stream=self.compute, gate_bias=gate_bias, workspace=self.ws)
+                            stream=self.compute, gate_bias=gate_bias, workspace=self.ws, gate_prep=gate_prep)
         self.fwd_done[s].record(self.compute)
         self.d2h.wait_event(self.fwd_done[s])
         with torch.cuda.stream(self.d2h):

@@ -237,7 +237,25 @@ typedef struct moe_forward_opts {
                                   workspace pair position, g at [p][c], u at [p][inter + c]),
                                   the tensor-core fp32 sums GEMM1 applies SwiGLU to; the
                                   input moe_backward_h needs.  NULL = not kept */
+    const void *gate_prep;     /* optional: moe_prepare_gate's buffer for this gate_w
+                                  (256-byte aligned).  From MOE_GATE_TC_MIN_TOKENS
+                                  tokens the forward then reads gate_w's split and
+                                  norms from it instead of computing them per call;
+                                  the results are the same bits.  NULL = compute */
 } moe_forward_opts;
+
+/*
+ * moe_prepare_gate -- gate_w's form for the tensor-core gate (large batches),
+ * computed once per gate_w like moe_pack_fp4's packed experts: gate_w
+ * transposed (fp32 [E][d]), split into bf16 high and low parts ([E][d] each),
+ * and an upper bound of each expert's weight norm (fp32 [E]).  Pass the buffer
+ * as moe_forward_opts.gate_prep; prepare again after changing gate_w.
+ *   gate_w  device fp32 [d][E], 16-byte aligned
+ *   prep    device, moe_gate_prep_size(d, E) bytes, 256-byte aligned
+ * Requires d % 128 == 0, 1 <= E <= 256.  Load-time operation.
+ */
+size_t moe_gate_prep_size(int d, int E);
+moe_status moe_prepare_gate(const float *gate_w, void *prep, int d, int E, void *stream);
 
 /* Test only (failure detection without a GPU fault): GEMM2 waits for a
  * GEMM1 completion count that is never published, before it issues any copy.

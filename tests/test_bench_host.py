@@ -30,18 +30,20 @@ def test_flop_identity_matches_cited_ratio():
 
 
 def test_kernels_per_step_follow_the_library_thresholds():
-    """gpu_launches claim: the gate and top-k (two kernels, or four on the
-    tensor-core path from 1024 tokens with E a multiple of 64), plan (one
-    kernel up to 32768 pairs, a count and a scatter kernel above), the
+    """gpu_launches claim: the gate and top-k (two kernels; on the tensor-core
+    path from 1024 tokens with E a multiple of 64 two more for gate_w's split
+    and norms unless they were prepared at load time, as the bench does), plan
+    (one kernel up to 32768 pairs, a count and a scatter kernel above), the
     expert-ordered copy (from 16 pairs per expert on average), GEMM1, GEMM2,
     combine."""
-    want = {"tiny": 6, "decode": 6, "mid": 9, "skew": 10, "prefill": 10}
+    want = {"tiny": 6, "decode": 6, "mid": 7, "skew": 8, "prefill": 8}
     for name, n in want.items():
         assert bench.kernels_per_step(inputs.WORKLOADS[name]) == n, name
+    assert bench.kernels_per_step(inputs.WORKLOADS["prefill"], gate_prepared=False) == 10
     edge = inputs.Workload("edge", T=4096, d=256, inter=128, E=256, k=8, seed=0)    # 32768 pairs: one plan kernel
-    assert bench.kernels_per_step(edge) == 9
+    assert bench.kernels_per_step(edge) == 7
     edge = inputs.Workload("edge", T=4097, d=256, inter=128, E=256, k=8, seed=0)    # 32776 pairs: two
-    assert bench.kernels_per_step(edge) == 10
+    assert bench.kernels_per_step(edge) == 8
     edge = inputs.Workload("edge", T=511, d=256, inter=128, E=256, k=8, seed=0)     # 4088 < 16 E: no copy
     assert bench.kernels_per_step(edge) == 6
     edge = inputs.Workload("edge", T=1023, d=256, inter=128, E=256, k=8, seed=0)    # below the tensor-core gate

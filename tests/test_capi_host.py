@@ -185,3 +185,17 @@ def test_backward_w_argument_checks(capi):
     assert lib.moe_backward_w(F, F, F, F, F, F, F, 16, 8, 256, 256, 8, 2, None) == 4        # workspace too small
     assert capi.moe_backward_w_workspace_size(8, 256, 384, 8, 2) == 0
     assert capi.moe_backward_w_workspace_size(8, 256, 256, 8, 2) > 0
+
+
+def test_prepare_gate_argument_checks(capi):
+    """moe_prepare_gate and moe_gate_prep_size reject bad shapes and pointers
+    before touching CUDA; the size covers the four parts, 256-byte aligned."""
+    lib = capi.lib()
+    F = 0x100000
+    assert capi.moe_gate_prep_size(320, 64) == 0                          # d % 128
+    assert capi.moe_gate_prep_size(256, 300) == 0                         # E > 256
+    d, E = 512, 64
+    assert capi.moe_gate_prep_size(d, E) == E * d * 4 + 2 * E * d * 2 + 256
+    assert lib.moe_prepare_gate(None, F, d, E, None) == 1
+    assert lib.moe_prepare_gate(F, F + 16, d, E, None) == 1              # prep alignment
+    assert lib.moe_prepare_gate(F, F, 320, E, None) == 2

@@ -137,3 +137,38 @@ def test_forward_tc_gate_workspace_and_layer(T, d, inter, E, k, case):
     f2, s2 = oracle.pack_fp4(w2.numpy())
     ref, _, _ = oracle.moe_forward(xb, gw, f13, s13, f2, s2, k, bias)
     check_layer_tolerance(inputs.bf16_bits(out), ref)
+
+
+@pytest.mark.parametrize("T,d,inter,E,k,case", [
+    (1100, 256, 128, 64, 6, "bias"),
+    (2000, 768, 128, 192, 4, "zero-rows"),
+])
+def test_forward_with_prepared_gate_is_the_same(T, d, inter, E, k, case):
+    """moe_forward_opts.gate_prep (gate_w's split and norms prepared once by
+    moe_prepare_gate): the same output and routing bits as computing them in
+    the call, and the prepared parts equal the ones a call leaves in its
+    workspace."""
+    from test_gpu_parity import small_case
+    from fp4_expert_grouped_gb300 import layer
+    c = capi()
+    _, _, _, _, w13, w2 = small_case(T, d, inter, E, k, seed=T + d)
+    x, gw, bias = make_gate_case(T, d, E, case, seed=T)
+    pk = layer.pack_experts(w13.to(DEV), w2.to(DEV))
+    xd, gd = x.to(DEV), torch.from_numpy(gw).to(DEV)
+    bd = None if bias is None else torch.from_numpy(bias).to(DEV)
+    ws = layer.workspace(T, d, inter, E, k, DEV)
+    out, ti, tw, pp = layer.forward(xd, gd, pk, k, gate_bias=bd, ws=ws, routing=True)
+    prep = layer.prepare_gate(gd)
+    ws2 = layer.workspace(T, d, inter, E, k, DEV)
+    out2, ti2, tw2, pp2 = layer.forward(xd, gd, pk, k, gate_bias=bd, ws=ws2, routing=True, gate_prep=prep)
+    assert c.moe_get_device_status() == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(ti, ti2) and torch.equal(tw.view(torch.int32), tw2.view(torch.int32)) and torch.equal(pp, pp2)
+    # the prepared parts are the bits a call computes into its workspace
+    _, off, _ = c.moe_workspace_layout(T, d, inter, E, k)
+    for name, nbytes in (("GATE_WT", E * d * 4), ("GATE_WHI", E * d * 2), ("GATE_WLO", E * d * 2), ("GATE_WNORM", E * 4)):
+        o = off[getattr(c, "MOE_WS_" + name)]
+        start = {"GATE_WT": 0, "GATE_WHI": 1, "GATE_WLO": 2, "GATE_WNORM": 3}[name]
+        sizes = [E * d * 4, E * d * 2, E * d * 2, E * 4]
+        po = sum((s + 255) // 256 * 256 for s in sizes[:start])
+        assert torch.equal(ws[o:o + nbytes], prep[po:po + nbytes]), name
