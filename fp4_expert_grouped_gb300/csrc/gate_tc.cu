@@ -112,7 +112,7 @@ constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
 constexpr int A_STAGE = BM * SK * 2;   // 8 KB of x
 
-template <int NH>                      // E = 64 * NH experts
+template <int NH>                      // 64 * NH experts per work unit
 struct Cfg {
     static constexpr int E = 64 * NH;
     static constexpr int B_STAGE = E * SK * 2;                 // hi (or lo) rows of one stage
@@ -135,17 +135,20 @@ struct Cfg {
     static_assert(B_STAGE % 512 == 0, "64-byte swizzle atoms stay aligned");
 };
 
-// Warp roles (320 threads): warp 0 producer (TMA loads of x and of the hi and
-// lo weight rows, 32 channels per stage), warp 1 tensor-memory owner and MMA
-// issuer (one thread: per stage two MMAs of K = 16 on hi, two on lo), warps
-// 2-9 epilogue (two per 32-lane quarter, each with half of the experts: per
-// 128-channel chunk, the buffer's fp32 sums added into registers; at the end
-// of the tile the bias is added and the row stored).
+// A work unit is 128 tokens x 64 * NH experts (column block cb of the E_all
+// experts); a small batch splits the experts over several units so that more
+// SMs stream the weights.  Warp roles (320 threads): warp 0 producer (TMA
+// loads of x and of the unit's hi and lo weight rows, 32 channels per stage),
+// warp 1 tensor-memory owner and MMA issuer (one thread: per stage two MMAs of
+// K = 16 on hi, two on lo), warps 2-9 epilogue (two per 32-lane quarter, each
+// with half of the unit's experts: per 128-channel chunk, the buffer's fp32
+// sums added into registers; at the end of the unit the bias is added and the
+// row stored).
 template <int NH>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmHi,
                    const __grid_constant__ CUtensorMap tmLo, const float *__restrict__ bias, float *__restrict__ approx,
-                   int T, int d, unsigned *status, unsigned long long timeout_ns)
+                   int T, int d, int E_all, unsigned *status, unsigned long long timeout_ns)
 {
     using C = Cfg<NH>;
     constexpr int E = C::E;
@@ -187,7 +190,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const int n_tiles = (T + BM - 1) / BM;
+    const int ncb = E_all / E;                   // column blocks per token tile
+    const int n_units = (T + BM - 1) / BM * ncb;
     const int nst = d / SK;                      // stages per tile
     const int nch = nst / CHUNK_STAGES;          // chunks per tile (d % 128 == 0)
 
@@ -196,7 +200,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             long long armed = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+                const int tile = u / ncb, e0 = (u - tile * ncb) * E;
                 for (int s = 0; s < nst; s++) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, timeout_ns, abort_flag)) {
                         *abort_flag = 1;
@@ -206,8 +211,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     armed++;
                     mbar_arrive_expect_tx(fb, C::STAGE_TX);
                     tma_load_2d(smem + C::OFF_A + stage * A_STAGE, &tmX, fb, s * SK, tile * BM);
-                    tma_load_2d(smem + C::OFF_BHI + stage * C::B_STAGE, &tmHi, fb, s * SK, 0);
-                    tma_load_2d(smem + C::OFF_BLO + stage * C::B_STAGE, &tmLo, fb, s * SK, 0);
+                    tma_load_2d(smem + C::OFF_BHI + stage * C::B_STAGE, &tmHi, fb, s * SK, e0);
+                    tma_load_2d(smem + C::OFF_BLO + stage * C::B_STAGE, &tmLo, fb, s * SK, e0);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t stage = 0, phase = 0, gc = 0;
             const uint32_t sbase = smem_u32(smem);
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < n_units && !*abort_flag; u += gridDim.x) {
                 for (int c = 0; ok && c < nch; c++, gc++) {
                     const uint32_t b = gc & 1u, use = gc >> 1;
                     if (!mbar_wait(&acc_empty[b], (use & 1u) ^ 1u, timeout_ns, abort_flag)) {
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = q * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * (E / 2));
         uint32_t gc = 0;
-        for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
             float sum[32 * NH];
 #pragma unroll
             for (int i = 0; i < 32 * NH; i++) sum[i] = 0.f;
@@ -301,17 +306,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 *abort_flag = 1;
                 break;
             }
+            const int tile = u / ncb, e0 = (u - tile * ncb) * E;
             const int t = tile * BM + r;
             if (t < T) {
-                float *dst = approx + (size_t)t * E + half * (E / 2);
+                float *dst = approx + (size_t)t * E_all + e0 + half * (E / 2);
 #pragma unroll
                 for (int i = 0; i < 32 * NH; i += 8) {
                     uint32_t w[8];
 #pragma unroll
-                    for (int u = 0; u < 8; u++) {
-                        float v = sum[i + u];
-                        if (bias) v = v + __ldg(bias + half * (E / 2) + i + u);
-                        w[u] = __float_as_uint(v);
+                    for (int m = 0; m < 8; m++) {
+                        float v = sum[i + m];
+                        if (bias) v = v + __ldg(bias + e0 + half * (E / 2) + i + m);
+                        w[m] = __float_as_uint(v);
                     }
                     st_global_v8(dst + i, w);
                 }
@@ -704,17 +710,43 @@ static bool make_map_bf16(CUtensorMap *m, const void *base, long long rows, int 
 
 template <int NH>
 static cudaError_t launch_gate_tc_cfg(const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &ml,
-                                      const float *bias, float *approx, int T, int d, int num_sms, unsigned *status,
-                                      unsigned long long timeout_ns, cudaStream_t st)
+                                      const float *bias, float *approx, int T, int d, int E, int num_sms,
+                                      unsigned *status, unsigned long long timeout_ns, cudaStream_t st)
 {
     using C = gtc::Cfg<NH>;
     auto kern = gtc::gate_tc_kernel<NH>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    const int tiles = (T + gtc::BM - 1) / gtc::BM;
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    return launch_pdl(kern, dim3(grid), dim3(gtc::NUM_THREADS), C::SMEM_BYTES, st, mx, mh, ml, bias, approx, T, d,
+    const int units = (T + gtc::BM - 1) / gtc::BM * (E / C::E);
+    const int grid = units < num_sms ? units : num_sms;
+    return launch_pdl(kern, dim3(grid), dim3(gtc::NUM_THREADS), C::SMEM_BYTES, st, mx, mh, ml, bias, approx, T, d, E,
                       status, timeout_ns);
+}
+
+// Experts per work unit (64 * NH of the E): each unit streams its 128 tokens'
+// x and its experts' hi and lo rows through one SM at the SM's copy rate, so
+// the launch takes about (units per SM, rounded up) x (x bytes + weight
+// bytes of a unit).  Splitting the experts pays when the token tiles alone
+// leave SMs idle: on 152 SMs with E = 256, 4096 tokens (32 tiles) run units
+// of 64 experts, 8192 tokens units of 128, 16384 tokens units of all 256.
+static int gate_tc_experts_per_unit(int T, int E, int num_sms)
+{
+    const long long tiles = (T + gtc::BM - 1) / gtc::BM;
+    int best = E;
+    long long best_cost = -1;
+    for (int ncb = 1; ncb <= 4; ncb *= 2) {
+        if (E % (64 * ncb) != 0) continue;
+        const int ecta = E / ncb;
+        const long long units = tiles * ncb;
+        const long long rounds = (units + num_sms - 1) / num_sms;
+        // per unit: x 128 rows x 2 bytes, weights ecta rows x 4 bytes (hi, lo)
+        const long long cost = rounds * (2LL * gtc::BM + 4LL * ecta);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = ecta;
+        }
+    }
+    return best;
 }
 
 cudaError_t launch_gate_prep(const float *gate_w, const GateScratch &g, int d, int E, cudaStream_t st)
@@ -736,15 +768,16 @@ cudaError_t launch_gate_tc_logits(const uint16_t *x, const float *gate_w, const 
         err = launch_gate_prep(gate_w, g, d, E, st);
         if (err != cudaSuccess) return err;
     }
+    const int ecta = gate_tc_experts_per_unit(T, E, num_sms);
     CUtensorMap mx, mh, ml;
-    if (!make_map_bf16(&mx, x, T, d, gtc::BM) || !make_map_bf16(&mh, g.whi, E, d, E) ||
-        !make_map_bf16(&ml, g.wlo, E, d, E))
+    if (!make_map_bf16(&mx, x, T, d, gtc::BM) || !make_map_bf16(&mh, g.whi, E, d, ecta) ||
+        !make_map_bf16(&ml, g.wlo, E, d, ecta))
         return cudaErrorInvalidValue;
-    switch (E / 64) {
-    case 1: err = launch_gate_tc_cfg<1>(mx, mh, ml, bias, g.approx, T, d, num_sms, status, timeout_ns, st); break;
-    case 2: err = launch_gate_tc_cfg<2>(mx, mh, ml, bias, g.approx, T, d, num_sms, status, timeout_ns, st); break;
-    case 3: err = launch_gate_tc_cfg<3>(mx, mh, ml, bias, g.approx, T, d, num_sms, status, timeout_ns, st); break;
-    default: err = launch_gate_tc_cfg<4>(mx, mh, ml, bias, g.approx, T, d, num_sms, status, timeout_ns, st); break;
+    switch (ecta / 64) {
+    case 1: err = launch_gate_tc_cfg<1>(mx, mh, ml, bias, g.approx, T, d, E, num_sms, status, timeout_ns, st); break;
+    case 2: err = launch_gate_tc_cfg<2>(mx, mh, ml, bias, g.approx, T, d, E, num_sms, status, timeout_ns, st); break;
+    case 3: err = launch_gate_tc_cfg<3>(mx, mh, ml, bias, g.approx, T, d, E, num_sms, status, timeout_ns, st); break;
+    default: err = launch_gate_tc_cfg<4>(mx, mh, ml, bias, g.approx, T, d, E, num_sms, status, timeout_ns, st); break;
     }
     return err;
 }
