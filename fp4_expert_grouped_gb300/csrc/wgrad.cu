@@ -38,7 +38,11 @@ constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr int OFF_BAR = OFF_B + STAGES * B_STAGE;
 constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 4 + 1) * 8;   // full/empty per stage, acc full/empty x2, drain
 constexpr int OFF_KB = OFF_MISC + 16;                           // kbase[E+1]
-constexpr int SMEM_USED = OFF_KB + (MAX_E + 1) * 4;
+// per epilogue warp, 32 rows x 32 fp32 columns: the accumulator rows, one per
+// lane, regrouped into whole 128-byte lines for the stores
+constexpr int STG_WARP = 32 * 32 * 4;
+constexpr int OFF_STG = (OFF_KB + (MAX_E + 1) * 4 + 127) / 128 * 128;
+constexpr int SMEM_USED = OFF_STG + EPI_WARPS * STG_WARP;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
 constexpr uint32_t TMEM_COLS = 512;        // two 256-column accumulators (no scale factors for bf16)
 // kind::f16, fp32 accumulator (bit 4), A and B bf16 (bits 7, 10), K-major, N = 256, M = 128
@@ -82,8 +86,11 @@ __global__ void __launch_bounds__(256) wg_kbase_kernel(const int32_t *__restrict
 
 // out[c][kcol] (bf16, row stride kp) = the dequantised operand of channel c of
 // the pair at padded column kcol (zero in padding columns).  A CTA transposes
-// a block of 64 columns x 64 channels through shared memory; every 64-column
-// block belongs to one expert.
+// a block of 64 columns x 256 channels through shared memory; every 64-column
+// block belongs to one expert.  Each thread loads four 16-byte pieces of one
+// pair's codes up front (a single piece per thread left the loads latency-bound:
+// about 0.55 of HBM).
+constexpr int kWgOpChannels = 256;
 __global__ void __launch_bounds__(256) wg_operand_kernel(WgSource src, const int32_t *__restrict__ kbase,
                                                          const int32_t *__restrict__ expert_offsets,
                                                          const int32_t *__restrict__ tile_prefix,
@@ -91,10 +98,10 @@ __global__ void __launch_bounds__(256) wg_operand_kernel(WgSource src, const int
                                                          long long kp, int width, int E, int k, int R)
 {
     pdl_wait();
-    __shared__ uint16_t tileT[64][64 + 2];        // [channel][column], padded against bank conflicts
+    __shared__ uint16_t tileT[kWgOpChannels][64 + 2];   // [channel][column], padded against bank conflicts
     __shared__ int s_e;
     const long long col0 = (long long)blockIdx.x * 64;
-    const int c0 = blockIdx.y * 64;
+    const int c0 = blockIdx.y * kWgOpChannels;
     if (col0 >= kbase[E]) return;                 // beyond the last expert's columns: never read
     if (threadIdx.x == 0) {
         int lo = 0, hi = E - 1;                   // the expert with kbase[e] <= col0 < kbase[e+1]
@@ -108,38 +115,49 @@ __global__ void __launch_bounds__(256) wg_operand_kernel(WgSource src, const int
     __syncthreads();
     const int e = s_e;
     const int n_e = expert_offsets[e + 1] - expert_offsets[e];
-    // load: thread t takes column i = t / 4 and channels 16 (t % 4) .. +16
+    // load: thread t takes column i = t / 4 and channels 16 (t % 4) + 64 j .. +16, j = 0..3
     {
         const int i = threadIdx.x >> 2, cq = (threadIdx.x & 3) * 16;
         const int local = (int)(col0 - kbase[e]) + i;
-        float v[16];
         if (local < n_e) {
             const long long pos = expert_offsets[e] + local;
             const long long row = src.by_token ? sorted_pair[pos] / k : pos;
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(src.codes + row * width + c0 + cq));
-            const int grp = (c0 + cq) / 128;
-            int s;
-            if (src.scale_stride) {
-                s = src.scale[row * src.scale_stride + grp];
-            } else {
-                const long long m = tile_prefix[e] + local / R;
-                s = src.scale[(m * stage_groups(width) + grp / 4) * kBlockScaleBytes + sf_byte(local % R, grp % 4)];
-            }
-            const float sc = exp2i(s - 127);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint4 raw[4];
 #pragma unroll
-            for (int u = 0; u < 16; u++) v[u] = e4m3_value((w[u >> 2] >> (8 * (u & 3))) & 0xFFu) * sc;
+            for (int j = 0; j < 4; j++)
+                raw[j] = __ldg(reinterpret_cast<const uint4 *>(src.codes + row * width + c0 + cq + 64 * j));
+            float sc[2];                              // the block's two 128-channel groups
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int grp = c0 / 128 + h;
+                int sb;
+                if (src.scale_stride) {
+                    sb = src.scale[row * src.scale_stride + grp];
+                } else {
+                    const long long m = tile_prefix[e] + local / R;
+                    sb = src.scale[(m * stage_groups(width) + grp / 4) * kBlockScaleBytes + sf_byte(local % R, grp % 4)];
+                }
+                sc[h] = exp2i(sb - 127);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+                for (int u = 0; u < 16; u++)
+                    tileT[64 * j + cq + u][i] = __bfloat16_as_ushort(
+                        __float2bfloat16_rn(e4m3_value((w[u >> 2] >> (8 * (u & 3))) & 0xFFu) * sc[j >> 1]));
+            }
         } else {
 #pragma unroll
-            for (int u = 0; u < 16; u++) v[u] = 0.f;
-        }
+            for (int j = 0; j < 4; j++)
 #pragma unroll
-        for (int u = 0; u < 16; u++) tileT[cq + u][i] = __bfloat16_as_ushort(__float2bfloat16_rn(v[u]));
+                for (int u = 0; u < 16; u++) tileT[64 * j + cq + u][i] = 0;
+        }
     }
     __syncthreads();
-    // store: 64 rows of 128 bytes, 16 bytes per thread and pass
+    // store: 256 rows of 128 bytes, 16 bytes per thread and pass
 #pragma unroll
-    for (int pass = 0; pass < 2; pass++) {
+    for (int pass = 0; pass < 8; pass++) {
         const int idx = threadIdx.x + pass * 256;
         const int c = idx >> 3, j = (idx & 7) * 8;
         uint32_t w[4];
@@ -291,8 +309,8 @@ __global__ void __launch_bounds__(wg::NUM_THREADS, 1)
             const int e = (int)(tile / (MB * NB)), rem = (int)(tile % (MB * NB));
             const int mb = rem / NB, nb = rem % NB;
             const int nk = (kb[e + 1] - kb[e]) / SK;
-            float *dst = out + ((size_t)e * Mout + (size_t)mb * BM + r) * Nout + (size_t)nb * BN + half * (BN / 2);
             if (nk == 0) {                            // an expert without pairs: zero gradient
+                float *dst = out + ((size_t)e * Mout + (size_t)mb * BM + r) * Nout + (size_t)nb * BN + half * (BN / 2);
                 const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
                 for (int i = 0; i < BN / 2; i += 8) st_global_v8(dst + i, z);
@@ -314,16 +332,33 @@ __global__ void __launch_bounds__(wg::NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[b]);
+            // Each lane holds one output row; stored as they are, every store
+            // instruction touched 32 lines (one sector each) and the stores
+            // throttled the kernel.  So each 32-column chunk goes through
+            // shared memory (16-byte units XOR-swizzled by the row: no bank
+            // conflicts either way) and comes back as row segments: four lanes
+            // per 128-byte line, eight whole lines per store instruction.
+            const uint32_t stg = smem_u32(smem + OFF_STG + (warp - 2) * STG_WARP);
+            float *const dst0 = out + ((size_t)e * Mout + (size_t)mb * BM + q * 32) * Nout + (size_t)nb * BN +
+                                half * (BN / 2);
+            const int rs = lane >> 2, ps = lane & 3;
 #pragma unroll
             for (int c = 0; c < 4; c++) {
                 const uint32_t *v = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
 #pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    uint32_t w[8];
+                for (int j = 0; j < 8; j++)
+                    st_shared_v4(stg + lane * 128 + 16 * (j ^ (lane & 7)), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                 v[4 * j + 3]);
+                __syncwarp();
 #pragma unroll
-                    for (int u = 0; u < 8; u++) w[u] = v[8 * j + u];
-                    st_global_v8(dst + 32 * c + 8 * j, w);
+                for (int i = 0; i < 4; i++) {
+                    const int rr = 8 * i + rs;
+                    uint32_t w[8];
+                    ld_shared_v4(stg + rr * 128 + 16 * ((2 * ps) ^ (rr & 7)), w[0], w[1], w[2], w[3]);
+                    ld_shared_v4(stg + rr * 128 + 16 * ((2 * ps + 1) ^ (rr & 7)), w[4], w[5], w[6], w[7]);
+                    st_global_v8(dst0 + (size_t)rr * Nout + 32 * c + 8 * ps, w);
                 }
+                __syncwarp();
             }
         }
     }
@@ -413,7 +448,7 @@ struct WgPlan {
 
 cudaError_t wg_operand(const WgPlan &pl, const WgSource &src, uint16_t *out, int width, cudaStream_t st)
 {
-    const dim3 grid((unsigned)(pl.cols / 64), (unsigned)(width / 64));
+    const dim3 grid((unsigned)(pl.cols / 64), (unsigned)(width / kWgOpChannels));
     return launch_pdl(wg_operand_kernel, grid, dim3(256), 0, st, src, (const int32_t *)pl.kbase, pl.offs,
                       pl.tile_prefix, pl.sorted_pair, out, pl.cols, width, pl.E, pl.k, pl.R);
 }
