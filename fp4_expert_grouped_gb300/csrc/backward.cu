@@ -48,57 +48,77 @@ __global__ void __launch_bounds__(256) bwd_scale_image_kernel(const uint8_t *__r
     pdl_trigger();
 }
 
-// dy of every pair in expert order, quantised: one warp per pair position.
-// dy = w_tj * dout_t in fp32, then E4M3 with one power-of-two scale per 128
-// channels (the activations' rule); the scale bytes go to the GEMM's per-tile
-// scale layout (row tiles of R pairs, as the forward's plan numbers them).
+// dy of every pair, quantised into expert order: one warp per token.  The
+// token's dout row is read once (a warp per pair position re-read it k times,
+// scattered, mostly from DRAM) and each of its k pairs gets dy = w_tj * dout_t
+// in fp32, then E4M3 with one power-of-two scale per 128 channels (the
+// activations' rule), written at the pair's expert-order position; the scale
+// bytes go to the GEMM's per-tile scale layout (row tiles of R pairs, as the
+// forward's plan numbers them).
 __global__ void __launch_bounds__(256) bwd_dy_kernel(const uint16_t *__restrict__ dout, const float *__restrict__ topk_w,
                                                      const int32_t *__restrict__ topk_idx,
-                                                     const int32_t *__restrict__ sorted_pair,
+                                                     const int32_t *__restrict__ pair_pos,
                                                      const int32_t *__restrict__ expert_offsets,
                                                      const int32_t *__restrict__ tile_prefix, uint8_t *__restrict__ dyq,
-                                                     uint8_t *__restrict__ dys_tiles, long long P, int d, int k, int R)
+                                                     uint8_t *__restrict__ dys_tiles, int T, int d, int k, int R)
 {
     pdl_wait();
-    const long long pos = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (pos >= P) return;
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
     const int lane = threadIdx.x & 31;
-    const int p = sorted_pair[pos];
-    const int t = p / k;
-    const int e = topk_idx[p];
-    const float w = topk_w[p];
-    const int local = (int)(pos - expert_offsets[e]);
-    const long long m = tile_prefix[e] + local / R;
-    const int r = local % R;
     const int G4 = stage_groups(d);
+    float w[8];
+    uint8_t *qrow[8];
+    uint8_t *srow[8];                                // the pair's scale byte of group 0
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        w[j] = 0.f;
+        qrow[j] = nullptr;
+        srow[j] = nullptr;
+        if (j < k) {
+            const int p = t * k + j;
+            const int pos = pair_pos[p];
+            const int e = topk_idx[p];
+            w[j] = topk_w[p];
+            const int local = pos - expert_offsets[e];
+            const long long m = tile_prefix[e] + local / R;
+            qrow[j] = dyq + (size_t)pos * d;
+            srow[j] = dys_tiles + (size_t)m * G4 * kBlockScaleBytes + sf_byte(local % R, 0);
+        }
+    }
     const uint4 *src = reinterpret_cast<const uint4 *>(dout + (size_t)t * d);
-    uint8_t *qrow = dyq + (size_t)pos * d;
     const int n8 = d / 8;
     for (int c = lane; c - lane < n8; c += 32) {
         uint4 cur = make_uint4(0, 0, 0, 0);
         if (c < n8) cur = __ldg(src + c);
         const uint32_t u[4] = {cur.x, cur.y, cur.z, cur.w};
-        float v[8];
+        float x[8];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            v[2 * i] = w * bf16_bits_to_f32(u[i] & 0xFFFFu);
-            v[2 * i + 1] = w * bf16_bits_to_f32(u[i] >> 16);
+            x[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
+            x[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
         }
-        float amax = 0.f;
+        const int grp = c / 16;                          // 128-channel group = K stage of the GEMM
 #pragma unroll
-        for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+        for (int j = 0; j < 8; j++) {
+            if (j >= k) break;
+            float v[8];
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        if (c < n8) {
-            const int ex = e4m3_scale_exp(amax);
-            const float sc = exp2i(-ex);
-            uint2 q;
-            q.x = cvt_e4m3x2(v[0] * sc, v[1] * sc) | (cvt_e4m3x2(v[2] * sc, v[3] * sc) << 16);
-            q.y = cvt_e4m3x2(v[4] * sc, v[5] * sc) | (cvt_e4m3x2(v[6] * sc, v[7] * sc) << 16);
-            reinterpret_cast<uint2 *>(qrow)[c] = q;
-            if ((lane & 15) == 0) {
-                const int grp = c / 16;                      // 128-channel group = K stage of the GEMM
-                dys_tiles[(m * G4 + grp / 4) * kBlockScaleBytes + sf_byte(r, grp % 4)] = (uint8_t)(ex + 127);
+            for (int i = 0; i < 8; i++) v[i] = w[j] * x[i];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            if (c < n8) {
+                const int ex = e4m3_scale_exp(amax);
+                const float sc = exp2i(-ex);
+                uint2 q;
+                q.x = cvt_e4m3x2(v[0] * sc, v[1] * sc) | (cvt_e4m3x2(v[2] * sc, v[3] * sc) << 16);
+                q.y = cvt_e4m3x2(v[4] * sc, v[5] * sc) | (cvt_e4m3x2(v[6] * sc, v[7] * sc) << 16);
+                reinterpret_cast<uint2 *>(qrow[j])[c] = q;
+                if ((lane & 15) == 0)
+                    srow[j][(size_t)(grp / 4) * kBlockScaleBytes + grp % 4] = (uint8_t)(ex + 127);
             }
         }
     }
@@ -265,7 +285,7 @@ extern "C" moe_status moe_backward_h(const uint16_t *dout, const uint8_t *w2_fp8
     const int32_t *topk_idx = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_TOPK_IDX]);
     const float *topk_w = reinterpret_cast<const float *>(fb + fw.off[MOE_WS_TOPK_W]);
     const int32_t *offs = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_EXPERT_OFFSETS]);
-    const int32_t *sorted_pair = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_SORTED_PAIR]);
+    const int32_t *pair_pos = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_PAIR_POS]);
     const int32_t *tile_prefix = reinterpret_cast<const int32_t *>(fb + fw.off[MOE_WS_TILE_PREFIX]);
     uint8_t *dyq = base + L.dyq, *dys = base + L.dys, *img = base + L.img;
 
@@ -273,8 +293,8 @@ extern "C" moe_status moe_backward_h(const uint16_t *dout, const uint8_t *w2_fp8
     cudaError_t e = launch_pdl(bwd_scale_image_kernel, dim3((unsigned)((n16 + 255) / 256)), dim3(256), 0, s, w2_s8t,
                                img, n16, inter, d);
     if (e == cudaSuccess)
-        e = launch_pdl(bwd_dy_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, s, dout, topk_w, topk_idx,
-                       sorted_pair, offs, tile_prefix, dyq, dys, P, d, k, R);
+        e = launch_pdl(bwd_dy_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, s, dout, topk_w, topk_idx,
+                       pair_pos, offs, tile_prefix, dyq, dys, T, d, k, R);
     if (e == cudaSuccess) {
         GemmArgs g;
         std::memset(&g, 0, sizeof g);
