@@ -928,7 +928,20 @@ __global__ void __launch_bounds__(NW * 32) plan_scatter_kernel(const int32_t *__
             before = pre[e];
             total = tot[e];
         } else if (cta_counts) {
-            for (int c = 0; c < C; c++) {
+            // the other CTAs' counts of expert e, sixteen loads in flight at a
+            // time (integer sums: any order gives the same totals)
+            int c = 0;
+            for (; c + 16 <= C; c += 16) {
+                int v[16];
+#pragma unroll
+                for (int u = 0; u < 16; u++) v[u] = __ldg(cta_counts + (size_t)(c + u) * E + e);
+#pragma unroll
+                for (int u = 0; u < 16; u++) {
+                    if (c + u < (int)blockIdx.x) before += v[u];
+                    total += v[u];
+                }
+            }
+            for (; c < C; c++) {
                 const int v = __ldg(cta_counts + (size_t)c * E + e);
                 if (c < (int)blockIdx.x) before += v;
                 total += v;
