@@ -82,17 +82,12 @@ cudaError_t launch_pack_fp4(const float *w, uint8_t *w_fp4, uint8_t *w_scale, in
 // block's largest 1x32 exponent - 6, at least -127), written transposed.
 // One CTA per block: the scales' maximum, the codes staged in shared memory,
 // then warp w writes the 16 codes of rows n = 16w .. 16w+15 of every output
-// row k as a 16-byte vector (lane = k % 32: the lanes read a shared 16-byte
-// span of one code row, so the reads broadcast).  code * 2^(X - B) is exact in fp32 down to its subnormals (it is
-// below E4M3's half-ulp, so rounds to a signed zero, whenever it is smaller),
-// and the E4M3 conversion rounds to nearest even.
+// row k as a 16-byte vector (lane q takes output rows 2q and 2q + 1, the two
+// codes of byte q of each code row, so the lanes read one shared 32-byte span
+// and the reads broadcast).  A value code * 2^(X - B) is exact in fp32 down to
+// its subnormals (it is below E4M3's half-ulp, so rounds to a signed zero,
+// whenever it is smaller), and the E4M3 conversion rounds to nearest even.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float e2m1_value(uint32_t code)
-{
-    const uint32_t e = (code >> 1) & 3u, m = code & 1u;
-    const uint32_t mag = e ? ((e + 126u) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
-    return __uint_as_float(mag | ((code & 8u) << 28));
-}
 
 // 2^e as fp32 for any e (subnormal, or zero below 2^-149)
 __device__ __forceinline__ float pow2_any(int e)
@@ -142,28 +137,39 @@ __global__ void __launch_bounds__(256) fp4_to_fp8t_kernel(const uint8_t *__restr
     for (int w = 1; w < 8; w++) S = max(S, s_max[w]);
     const int B = max(S - 6, -127);
     if (t == 0) s8t[((long long)e * KB + bk) * NB + bn] = (uint8_t)(B + 127);
-    // output rows k of the block, 16 codes (16 rows n) per lane
+    // Every 32-code sub-block (row n, sub-block j of K) shares one shift
+    // X - B, so the E4M3 codes of its eight magnitudes {0, .5, 1, 1.5, 2, 3,
+    // 4, 6} x 2^(X-B) are converted once into a table (the same products and
+    // the same conversion as code by code); a code is then a byte select plus
+    // its sign bit (E4M3 is sign-symmetric, -0 included).
+    __shared__ uint2 lut[128 * 4];
+    for (int i = t; i < 128 * 4; i += 256) {
+        const int n = i >> 2, j = i & 3;
+        const float p = pow2_any((int)sc[sf_byte(n, j)] - 127 - B);
+        lut[i] = make_uint2(cvt_e4m3x2(0.f * p, 0.5f * p) | (cvt_e4m3x2(1.f * p, 1.5f * p) << 16),
+                            cvt_e4m3x2(2.f * p, 3.f * p) | (cvt_e4m3x2(4.f * p, 6.f * p) << 16));
+    }
+    __syncthreads();
+    // output rows k = 2q and 2q + 1 of the block (both codes of one byte),
+    // 16 codes (16 rows n) per lane and row
     const int n0 = warp * 16;
-    for (int k = lane; k < 128; k += 32) {
-        const int j = k >> 5;                     // 32-element sub-block of K
-        uint32_t out[4];
+    for (int q = lane; q < 64; q += 32) {
+        const int j = q >> 4;                     // 32-element sub-block of K
+        uint32_t out0[4] = {0, 0, 0, 0}, out1[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
-            float v2[2];
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const int n = n0 + 2 * u + h;
-                const uint32_t byte = codes[n * kF8tRow + (k >> 1)];
-                const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
-                const int X = (int)sc[sf_byte(n, j)] - 127;
-                v2[h] = e2m1_value(code) * pow2_any(X - B);
-            }
-            const uint32_t c2 = cvt_e4m3x2(v2[0], v2[1]);
-            if (u & 1) out[u >> 1] |= c2 << 16;
-            else out[u >> 1] = c2;
+        for (int u = 0; u < 16; u++) {
+            const int n = n0 + u;
+            const uint32_t byte = codes[n * kF8tRow + q];
+            const uint2 L = lut[n * 4 + j];
+            const uint32_t lo = byte & 15u, hi = byte >> 4;
+            const uint32_t c0 = (__byte_perm(L.x, L.y, lo & 7u) & 0xFFu) | ((lo & 8u) << 4);
+            const uint32_t c1 = (__byte_perm(L.x, L.y, hi & 7u) & 0xFFu) | ((hi & 8u) << 4);
+            out0[u >> 2] |= c0 << (8 * (u & 3));
+            out1[u >> 2] |= c1 << (8 * (u & 3));
         }
-        uint8_t *dst = w8t + fp8t_block(e, bk, bn, K, N) * kF8tBlockBytes + k * 128 + n0;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+        uint8_t *dst = w8t + fp8t_block(e, bk, bn, K, N) * kF8tBlockBytes + (2 * q) * 128 + n0;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(out0[0], out0[1], out0[2], out0[3]);
+        *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(out1[0], out1[1], out1[2], out1[3]);
     }
     pdl_trigger();
 }
