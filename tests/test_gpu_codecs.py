@@ -116,13 +116,34 @@ def test_fp4_to_fp8t_bitexact(E, N, K):
     block) from the GPU pack: the oracle's codes and block exponents bit for bit,
     on trained-like weights, an all-zero block and a block whose sub-block
     scales span more than 2^14 (rounded, not lossless)."""
-    c = capi()
     rng = np.random.default_rng(E * N + K)
     w = (rng.normal(0, 1, (E, N, K)) / np.sqrt(K)).astype(np.float32)
     w[0, :128, :128] = 0.0
     if E > 1:
         w[E - 1, 128:256, 128:160] = rng.uniform(-300, 300, (128, 32))
         w[E - 1, 128:256, 160:192] = rng.uniform(-1, 1, (128, 32)) * 2.0 ** -16
+    check_fp4_to_fp8t(w)
+
+
+def test_fp4_to_fp8t_bitexact_scale_spread():
+    """Every 1x32 sub-block at its own power of two, 2^-24 .. 2^8, so that inside
+    each 128x128 block the shifts X - B run from 0 down far past E4M3's
+    subnormals: exact codes, round-to-nearest-even below 2^-6, underflow to a
+    signed zero; and one sub-block of every E2M1 value at both signs.  Bit-exact
+    with the oracle."""
+    rng = np.random.default_rng(2024)
+    E, N, K = 2, 256, 512
+    w = rng.normal(0, 1, (E, N, K)).astype(np.float32)
+    shift = rng.integers(-24, 9, (E, N, K // 32))
+    w *= np.repeat(np.exp2(shift.astype(np.float64)), 32, axis=2).astype(np.float32)
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float32)
+    w[1, 5, 64:96] = np.concatenate([vals, -vals, vals * 4, -vals * 4])
+    check_fp4_to_fp8t(w)
+
+
+def check_fp4_to_fp8t(w):
+    c = capi()
+    E, N, K = w.shape
     wd = torch.from_numpy(w).to(DEV)
     fp4 = torch.empty((E, N, K // 2), dtype=torch.uint8, device=DEV)
     sc = torch.empty((E, N, K // 32), dtype=torch.uint8, device=DEV)
